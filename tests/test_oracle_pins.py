@@ -1,0 +1,403 @@
+"""Pins of the CPU oracle against facts that do not come from the oracle itself.
+
+Each test ties one part of the oracle to something fixed outside it: the FP8
+format table of the page "DeepGEMM: FP8 GEMM on Hopper" (section 3.1), hand
+decoded bytes, torch's float8/bfloat16 conversions, numpy's float64 matmul on
+the unit-scale special case, closed forms, brute force over all FP8 codes and
+invariants of the definition (zero scales, power-of-two linearity, grouped
+layouts equal per-group dense calls).  No GPU is used.
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as wl
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _golden_formats():
+    rows = {}
+    with open(os.path.join(GOLDEN, "fp8_formats.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            name, s, e, m, mx = line.split()
+            rows[name] = (int(s), int(e), int(m), float(mx))
+    return rows
+
+
+# ------------------------------------------------------------------ decoding
+
+@pytest.mark.parametrize("code,val", [
+    (0x38, 1.0), (0x7E, 448.0), (0xFE, -448.0), (0x01, 2.0 ** -9), (0x07, 7 * 2.0 ** -9),
+    (0x08, 2.0 ** -6), (0x00, 0.0), (0x40, 2.0), (0x3C, 1.5), (0x30, 0.5), (0xB8, -1.0),
+])
+def test_e4m3_hand_decoded(code, val):
+    assert oracle.decode(oracle.E4M3, code) == val
+
+
+def test_e4m3_signed_zero_and_nan():
+    z = oracle.decode(oracle.E4M3, 0x80)
+    assert z == 0.0 and math.copysign(1.0, z) == -1.0
+    assert math.isnan(oracle.decode(oracle.E4M3, 0x7F))
+    assert math.isnan(oracle.decode(oracle.E4M3, 0xFF))
+
+
+@pytest.mark.parametrize("code,val", [
+    (0x7B, 57344.0), (0x01, 2.0 ** -16), (0x3C, 1.0), (0x7C, math.inf), (0xFC, -math.inf),
+    (0x04, 2.0 ** -14), (0xBC, -1.0), (0x3E, 1.5),
+])
+def test_e5m2_hand_decoded(code, val):
+    assert oracle.decode(oracle.E5M2, code) == val
+
+
+def test_e5m2_nans():
+    for c in (0x7D, 0x7E, 0x7F, 0xFD, 0xFE, 0xFF):
+        assert math.isnan(oracle.decode(oracle.E5M2, c))
+
+
+@pytest.mark.parametrize("name,fmt", [("E4M3", oracle.E4M3), ("E5M2", oracle.E5M2)])
+def test_formats_match_page_table(name, fmt):
+    """Largest finite value and the exponent/mantissa widths of the page's table."""
+    sign, ebits, mbits, mx = _golden_formats()[name]
+    t = oracle.decode_table(fmt)
+    fin = t[np.isfinite(t)]
+    assert fin.max() == mx and fin.min() == -mx
+    # positive codes: the upper bit is the sign
+    assert sign == 1 and all(oracle.decode(fmt, c) == -oracle.decode(fmt, c | 0x80)
+                             for c in range(0x80) if np.isfinite(t[c]) and t[c] != 0)
+    # within one binade, consecutive codes differ by 2^-mbits relative
+    one = [c for c in range(0x80) if t[c] == 1.0][0]
+    assert t[one + 1] == 1.0 + 2.0 ** -mbits
+    # the smallest normal is 2^(1 - bias), bias = 2^(ebits-1) - 1
+    bias = 2 ** (ebits - 1) - 1
+    smallest_normal = t[1 << mbits]
+    assert smallest_normal == 2.0 ** (1 - bias)
+    # the smallest subnormal is one mantissa step below that
+    assert t[1] == 2.0 ** (1 - bias - mbits)
+
+
+@pytest.mark.parametrize("fmt,tdt", [(oracle.E4M3, torch.float8_e4m3fn), (oracle.E5M2, torch.float8_e5m2)])
+def test_decode_matches_torch_float8(fmt, tdt):
+    ref = torch.arange(256, dtype=torch.uint8).view(tdt).to(torch.float64).numpy()
+    ours = oracle.decode_table(fmt)
+    both_nan = np.isnan(ref) & np.isnan(ours)
+    assert np.all(both_nan | (ref == ours))
+    assert np.array_equal(np.signbit(ref[~both_nan]), np.signbit(ours[~both_nan]))
+
+
+@pytest.mark.parametrize("fmt", [oracle.E4M3, oracle.E5M2])
+def test_encode_decode_roundtrip(fmt):
+    """The input generator's encoder inverts the oracle's decoder on every finite code."""
+    t = oracle.decode_table(fmt)
+    codes = np.array([c for c in range(256) if np.isfinite(t[c])], np.uint8)
+    vals = t[codes].astype(np.float32)
+    back = wl.encode_fp8(vals, fmt)
+    # -0 and +0 both decode to zero; compare values for those, codes elsewhere
+    nz = vals != 0
+    assert np.array_equal(back[nz], codes[nz])
+    assert np.all(t[back[~nz]] == 0)
+
+
+# ------------------------------------------------------------ bf16 rounding
+
+@pytest.mark.parametrize("x,bits", [
+    (1.0, 0x3F80), (-2.0, 0xC000), (0.0, 0x0000),
+    (1.0 + 2.0 ** -8, 0x3F80),            # tie, even stays
+    (1.0 + 3 * 2.0 ** -8, 0x3F82),        # tie, rounds up to even
+    (1.0 + 2.0 ** -8 + 2.0 ** -30, 0x3F81),  # just above the tie: direct rounding from FP64
+    (1.0 + 2.0 ** -9, 0x3F80),
+    (255 * 2.0 ** 120, 0x7F7F),           # largest finite
+    (2.0 ** 128, 0x7F80), (-1e300, 0xFF80),
+    (255 * 2.0 ** 120 + 2.0 ** 119, 0x7F80),  # tie above max goes to inf (max is odd)
+    (2.0 ** -126, 0x0080), (2.0 ** -133, 0x0001), (2.0 ** -134, 0x0000),
+    (3 * 2.0 ** -134, 0x0002), (127 * 2.0 ** -133, 0x007F),
+])
+def test_bf16_rne_hand_cases(x, bits):
+    assert oracle.bf16_rne(x) == bits
+
+
+def test_bf16_rne_negative_zero_and_nan():
+    assert oracle.bf16_rne(-0.0) == 0x8000
+    assert oracle.bf16_rne(float("nan")) == 0x7FC0
+    assert oracle.bf16_rne(float("inf")) == 0x7F80
+
+
+def test_bf16_rne_matches_torch_on_float32_inputs():
+    """On values exactly representable in float32, direct rounding from FP64
+    equals torch's float32 -> bfloat16 round-to-nearest-even."""
+    rng = np.random.default_rng(7)
+    x = np.concatenate([
+        rng.standard_normal(4000).astype(np.float32) * np.float32(1000.0),
+        (rng.standard_normal(2000) * 1e-39).astype(np.float32),  # subnormal float32 range
+        np.float32(1.0) + np.arange(512, dtype=np.float32) * np.float32(2.0 ** -16),
+    ])
+    ref = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().astype(np.uint16)
+    ours = np.array([oracle.bf16_rne(float(v)) for v in x], np.uint16)
+    assert np.array_equal(ref, ours)
+
+
+# -------------------------------------------------------------- the GEMM
+
+def _dec(codes, fmt):
+    return oracle.decode_table(fmt)[np.asarray(codes, np.int64)]
+
+
+def _bits_to_f(bits):
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).float().numpy()
+
+
+def test_unit_scales_equal_numpy_matmul_exactly():
+    """Scales of one reduce the definition to a plain matmul; for E4M3 every
+    partial sum is exact in FP64, so any summation order gives the same bits."""
+    p = wl.dense(37, 300, 400, seed=11)  # partial last K block (400 = 3*128 + 16)
+    sA = np.ones_like(p.sA)
+    sB = np.ones_like(p.sB)
+    d16, d64 = oracle.gemm_fp8_nt(p.A, 0, sA, p.B, 0, sB)
+    ref = _dec(p.A, 0) @ _dec(p.B, 0).T
+    assert np.array_equal(d64, ref)
+    # where the sum is exact in float32, torch's float32 -> bfloat16 rounding
+    # is a second, independent rounding of the same value
+    exact32 = ref.astype(np.float32).astype(np.float64) == ref
+    assert exact32.mean() > 0.2
+    ref16 = torch.from_numpy(ref.astype(np.float32)).to(torch.bfloat16).view(torch.int16).numpy()
+    assert np.array_equal(d16.view(np.int16)[exact32], ref16[exact32])
+
+
+def test_row_and_column_block_scales_equal_scaled_numpy_matmul():
+    """Scales constant along K (power-of-two per row, per 128-column block):
+    D = diag(sA) (A B^T) diag(sB), exact in FP64."""
+    rng = np.random.default_rng(3)
+    p = wl.dense(20, 260, 256, seed=12)
+    ra = np.exp2(rng.integers(-6, 7, size=20)).astype(np.float32)
+    rb = np.exp2(rng.integers(-6, 7, size=3)).astype(np.float32)
+    sA = np.repeat(ra[:, None], 2, axis=1)
+    sB = np.repeat(rb[:, None], 2, axis=1)
+    _, d64 = oracle.gemm_fp8_nt(p.A, 0, sA, p.B, 0, sB)
+    col_scale = rb[np.arange(260) // 128].astype(np.float64)
+    ref = (ra.astype(np.float64)[:, None] * (_dec(p.A, 0) @ _dec(p.B, 0).T)) * col_scale[None, :]
+    assert np.array_equal(d64, ref)
+
+
+def test_mixed_e4m3_e5m2_unit_scales_close_to_numpy():
+    p = wl.dense(16, 64, 256, seed=13, b_fmt=wl.E5M2)
+    _, d64 = oracle.gemm_fp8_nt(p.A, 0, np.ones_like(p.sA), p.B, 1, np.ones_like(p.sB))
+    ref = _dec(p.A, 0) @ _dec(p.B, 1).T
+    np.testing.assert_allclose(d64, ref, rtol=1e-14, atol=0)
+
+
+def test_brute_force_all_code_pairs_k1():
+    """k = 1: every E4M3 x E4M3 code pair times power-of-two scales, against
+    torch's decode and torch's float32 -> bfloat16 rounding (the product of two
+    FP8 values has at most 8 significant bits, so float32 holds it exactly)."""
+    codes = np.array([c for c in range(256) if c not in (0x7F, 0xFF)], np.uint8)
+    A = codes.reshape(-1, 1)
+    B = codes.reshape(-1, 1)
+    rng = np.random.default_rng(5)
+    sA = np.exp2(rng.integers(-4, 5, size=(len(codes), 1))).astype(np.float32)
+    sB = np.exp2(rng.integers(-4, 5, size=(2, 1))).astype(np.float32)
+    d16, d64 = oracle.gemm_fp8_nt(A, 0, sA, B, 0, sB)
+    tv = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    colsc = sB[np.arange(len(codes)) // 128, 0].astype(np.float64)
+    ref = (tv[:, None] * tv[None, :]) * (sA.astype(np.float64) * colsc[None, :])
+    assert np.array_equal(d64, ref)
+    ref16 = torch.from_numpy(ref.astype(np.float32)).to(torch.bfloat16).view(torch.int16).numpy()
+    ref16 = ref16.view(np.uint16)
+    # the sign of a zero result is not part of the definition (a sum that
+    # starts from +0 turns -0 products into +0): compare zeros as zeros
+    def unsign0(b):
+        return np.where((b & 0x7FFF) == 0, 0, b)
+    assert np.array_equal(unsign0(d16), unsign0(ref16))
+
+
+def test_closed_form_all_ones():
+    """A = B = 1.0 everywhere with uniform scales a, b: D = k * a * b."""
+    m, n, k = 5, 136, 384
+    A = np.full((m, k), 0x38, np.uint8)
+    B = np.full((n, k), 0x38, np.uint8)
+    sA = np.full((m, 3), 0.75, np.float32)
+    sB = np.full((2, 3), 2.5, np.float32)
+    d16, d64 = oracle.gemm_fp8_nt(A, 0, sA, B, 0, sB)
+    assert np.all(d64 == k * 0.75 * 2.5)
+    assert np.all(_bits_to_f(d16) == 720.0)
+
+
+def test_closed_form_geometric_lhs_scales():
+    """sA[m,kb] = 2^kb with ones: D = 128 * sB * (2^KB - 1)."""
+    KB = 6
+    m, n, k = 3, 128, 128 * KB
+    A = np.full((m, k), 0x38, np.uint8)
+    B = np.full((n, k), 0x38, np.uint8)
+    sA = np.tile(np.exp2(np.arange(KB)).astype(np.float32), (m, 1))
+    sB = np.full((1, KB), 0.5, np.float32)
+    _, d64 = oracle.gemm_fp8_nt(A, 0, sA, B, 0, sB)
+    assert np.all(d64 == 128 * 0.5 * (2 ** KB - 1))
+
+
+def test_one_hot_selects_the_right_scale_entries():
+    """Row r of A holds a single 1.0 at column kr; B is all ones.  Then
+    D[r, c] = sA[r, kr // 128] * sB[c // 128, kr // 128]: a transposed or
+    shifted scale index picks another entry and fails."""
+    m, n, k = 3, 300, 384        # 3 N-blocks, 3 K-blocks, non-square scale grids
+    kr = [5, 200, 300]
+    A = np.zeros((m, k), np.uint8)
+    for r in range(m):
+        A[r, kr[r]] = 0x38
+    B = np.full((n, k), 0x38, np.uint8)
+    sA = (np.arange(m * 3, dtype=np.float32).reshape(m, 3) + 1) * np.float32(0.5)
+    sB = (np.arange(9, dtype=np.float32).reshape(3, 3) + 1) * np.float32(4.0)
+    _, d64 = oracle.gemm_fp8_nt(A, 0, sA, B, 0, sB)
+    for r in range(m):
+        kb = kr[r] // 128
+        for c in (0, 127, 128, 255, 256, 299):
+            assert d64[r, c] == float(sA[r, kb]) * float(sB[c // 128, kb])
+
+
+def test_one_hot_on_b_selects_the_right_column():
+    """B row c holds a single value at column kc; A is all ones.  A swapped
+    operand (A[m] paired with B[m]) fails this."""
+    m, n, k = 4, 8, 256
+    A = np.full((m, k), 0x38, np.uint8)
+    B = np.zeros((n, k), np.uint8)
+    vals = [0x40, 0x44, 0x48, 0x30, 0xB8, 0x3C, 0x7E, 0x01]  # 2, 3, 4, .5, -1, 1.5, 448, 2^-9
+    for c in range(n):
+        B[c, (c * 37) % k] = vals[c]
+    sA = np.ones((m, 2), np.float32)
+    sB = np.ones((1, 2), np.float32)
+    _, d64 = oracle.gemm_fp8_nt(A, 0, sA, B, 0, sB)
+    for c in range(n):
+        assert np.all(d64[:, c] == oracle.decode(0, vals[c]))
+
+
+def test_zero_scale_block_equals_zeroed_payload():
+    p = wl.dense(9, 200, 512, seed=14)
+    sA = p.sA.copy()
+    sA[:, 2] = 0.0
+    A2 = p.A.copy()
+    A2[:, 256:384] = 0
+    _, d_a = oracle.gemm_fp8_nt(p.A, 0, sA, p.B, 0, p.sB)
+    _, d_b = oracle.gemm_fp8_nt(A2, 0, p.sA, p.B, 0, p.sB)
+    assert np.array_equal(d_a, d_b)
+    sB = p.sB.copy()
+    sB[1, :] = 0.0
+    _, d_c = oracle.gemm_fp8_nt(p.A, 0, p.sA, p.B, 0, sB)
+    assert np.all(d_c[:, 128:200] == 0.0)
+    d16, d_z = oracle.gemm_fp8_nt(p.A, 0, np.zeros_like(p.sA), p.B, 0, p.sB)
+    assert np.all(d_z == 0.0) and np.all((d16 & 0x7FFF) == 0)
+
+
+def test_power_of_two_scale_linearity_is_bitwise():
+    p = wl.dense(17, 130, 640, seed=15)
+    d16, d64 = oracle.gemm_fp8_nt(p.A, 0, p.sA, p.B, 0, p.sB)
+    for e in (-3, 1, 5):
+        s = np.float32(2.0 ** e)
+        e16, e64 = oracle.gemm_fp8_nt(p.A, 0, p.sA * s, p.B, 0, p.sB)
+        assert np.array_equal(e64, d64 * float(s))
+        f16, f64 = oracle.gemm_fp8_nt(p.A, 0, p.sA, p.B, 0, p.sB * s)
+        assert np.array_equal(f64, d64 * float(s))
+        assert np.array_equal(_bits_to_f(e16), _bits_to_f(d16) * float(s))
+
+
+def test_sampled_positions_equal_full_result():
+    p = wl.dense(70, 264, 272, seed=16)
+    d16, d64 = oracle.gemm_fp8_nt(p.A, 0, p.sA, p.B, 0, p.sB)
+    rng = np.random.default_rng(1)
+    rows = rng.integers(0, 70, 500)
+    cols = rng.integers(0, 264, 500)
+    s16, s64 = oracle.gemm_fp8_nt_at(p.A, 0, p.sA, p.B, 0, p.sB, rows, cols)
+    assert np.array_equal(s64, d64[rows, cols]) and np.array_equal(s16, d16[rows, cols])
+
+
+def test_bf16_output_is_rounding_of_f64_output():
+    p = wl.dense(8, 64, 256, seed=17)
+    d16, d64 = oracle.gemm_fp8_nt(p.A, 0, p.sA, p.B, 0, p.sB)
+    assert all(oracle.bf16_rne(float(v)) == int(b) for v, b in zip(d64.ravel(), d16.ravel()))
+
+
+# --------------------------------------------------------- grouped layouts
+
+SENTINEL = 0xFFFF
+
+
+def test_contiguous_equals_per_group_dense_and_leaves_padding():
+    p = wl.contiguous([100, 0, 130, 5], n=136, k=272, seed=18)
+    assert p.M == 128 + 0 + 256 + 128
+    init = np.full((p.M, p.n), SENTINEL, np.uint16)
+    d16, d64 = oracle.grouped_contiguous(p.A, 0, p.sA, p.B, 0, p.sB, p.m_indices, init, want_f64=True)
+    for g in range(p.G):
+        rows = np.nonzero(p.m_indices == g)[0]
+        if rows.size == 0:
+            continue
+        e16, e64 = oracle.gemm_fp8_nt(p.A[rows], 0, p.sA[rows], p.B[g], 0, p.sB[g])
+        assert np.array_equal(d16[rows], e16) and np.array_equal(d64[rows], e64)
+    pad = p.m_indices < 0
+    assert pad.sum() == p.M - 235
+    assert np.all(d16[pad] == SENTINEL)
+
+
+def test_contiguous_out_of_range_group_ids_leave_rows_untouched():
+    p = wl.contiguous([128, 128], n=64, k=128, seed=23)
+    mi = p.m_indices.copy()
+    mi[128:] = 2          # == G: not a group
+    mi[5] = 99
+    init = np.full((p.M, p.n), SENTINEL, np.uint16)
+    d16, _ = oracle.grouped_contiguous(p.A, 0, p.sA, p.B, 0, p.sB, mi, init)
+    assert np.all(d16[128:] == SENTINEL) and np.all(d16[5] == SENTINEL)
+    assert not np.any(d16[:5] == SENTINEL)
+    s16, _ = oracle.grouped_contiguous_at(p.A, 0, p.sA, p.B, 0, p.sB, mi, [5, 130], [0, 1])
+    assert np.all(s16 == SENTINEL)
+
+
+def test_contiguous_sampled_equals_full():
+    p = wl.contiguous([60, 128], n=64, k=128, seed=19)
+    init = np.full((p.M, p.n), SENTINEL, np.uint16)
+    d16, _ = oracle.grouped_contiguous(p.A, 0, p.sA, p.B, 0, p.sB, p.m_indices, init)
+    rows = np.arange(p.M).repeat(3)
+    cols = np.tile([0, 31, 63], p.M)
+    s16, _ = oracle.grouped_contiguous_at(p.A, 0, p.sA, p.B, 0, p.sB, p.m_indices, rows, cols)
+    assert np.array_equal(s16, d16[rows, cols])
+
+
+def test_masked_equals_per_group_dense_and_leaves_rest():
+    p = wl.masked(3, 96, n=128, k=256, seed=20, masked_m=[0, 96, 37])
+    init = np.full((p.G, p.M_cap, p.n), SENTINEL, np.uint16)
+    d16, _ = oracle.grouped_masked(p.A, 0, p.sA, p.B, 0, p.sB, p.masked_m, init)
+    for g in range(p.G):
+        v = int(p.masked_m[g])
+        if v:
+            e16, _ = oracle.gemm_fp8_nt(p.A[g, :v], 0, p.sA[g, :v], p.B[g], 0, p.sB[g])
+            assert np.array_equal(d16[g, :v], e16)
+        assert np.all(d16[g, v:] == SENTINEL)
+
+
+def test_masked_counts_are_clamped():
+    p = wl.masked(2, 64, n=64, k=128, seed=21, masked_m=[-5, 1000])
+    init = np.full((2, 64, 64), SENTINEL, np.uint16)
+    d16, _ = oracle.grouped_masked(p.A, 0, p.sA, p.B, 0, p.sB, p.masked_m, init)
+    assert np.all(d16[0] == SENTINEL)
+    e16, _ = oracle.gemm_fp8_nt(p.A[1], 0, p.sA[1], p.B[1], 0, p.sB[1])
+    assert np.array_equal(d16[1], e16)
+
+
+def test_masked_sampled_equals_full():
+    p = wl.masked(2, 64, n=64, k=128, seed=22, masked_m=[10, 64])
+    init = np.full((2, 64, 64), SENTINEL, np.uint16)
+    d16, _ = oracle.grouped_masked(p.A, 0, p.sA, p.B, 0, p.sB, p.masked_m, init)
+    g = np.repeat([0, 1], 64 * 2)
+    r = np.tile(np.repeat(np.arange(64), 2), 2)
+    c = np.tile([3, 60], 128)
+    s16, _ = oracle.grouped_masked_at(p.A, 0, p.sA, p.B, 0, p.sB, p.masked_m, g, r, c)
+    assert np.array_equal(s16, d16[g, r, c])
+
+
+def test_oracle_rejects_bad_shapes():
+    A = np.zeros((2, 0), np.uint8)
+    with pytest.raises(ValueError):
+        oracle.gemm_fp8_nt(A, 0, np.zeros((2, 0), np.float32), np.zeros((2, 0), np.uint8), 0,
+                           np.zeros((1, 0), np.float32))
