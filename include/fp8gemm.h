@@ -1,0 +1,133 @@
+/*
+ * fp8gemm.h -- C ABI of the GB300 (sm_103a) FP8 NT GEMM library.
+ *
+ * The operation (page "DeepSeek开源周第三天DeepGEMM", sections "核心功能",
+ * "基本用法" and the promotion excerpt "两级精度累加与细粒度缩放"):
+ *
+ *   D[m,n] = bf16( sum_kb sA[m,kb] * sB[n/128,kb] * sum_{k in kb} A[m,k] * B[n,k] )
+ *
+ * A (LHS) is an FP8 m x k matrix, B (RHS) an FP8 n x k matrix (both K-major:
+ * the "NT" layout, B is stored transposed), sA holds one FP32 scale per row
+ * and 128-wide K block (1x128 groups), sB one FP32 scale per 128x128 block.
+ * kb runs over ceil(k/128) K blocks.  Each K block is multiplied on the tensor
+ * cores into a fresh FP32 partial, which is then scaled by sA*sB and added to
+ * an FP32 running sum on the CUDA cores (the page's two-level accumulation).
+ * The output is BF16, rounded to nearest even.
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * - All pointers named A, B, sA, sB, D, m_indices, masked_m are DEVICE
+ *   pointers owned by the caller; the library keeps no reference after the
+ *   call returns.
+ * - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *   Calls are asynchronous on that stream: they allocate nothing, never
+ *   synchronize the host and read no device data on the host, so they can be
+ *   captured in a CUDA graph.
+ * - FP8 formats: FG_E4M3 (float8 e4m3 "fn": max 448, no infinities) or
+ *   FG_E5M2 (max 57344).  A and B may use different formats.
+ * - Layouts (row-major, leading dimension = row length unless stated):
+ *     A   [rows][k] bytes                      16-byte aligned, k % 16 == 0
+ *     B   [G][n][k] bytes (dense: G = 1)       16-byte aligned
+ *     sA  MN-major: [kb][ld_sA] floats, i.e. the scales of K block kb for all
+ *         rows are contiguous (masked layout: [G][kb][ld_sA]);
+ *         ld_sA >= rows (M_cap for masked), ld_sA % 4 == 0.  Entries past the
+ *         rows are never read.  fg_scales_a_to_mn_major() builds this layout
+ *         from the row-major [rows][kb] one.
+ *     sB  [G][ceil(n/128)][ceil(k/128)] floats, row-major
+ *     D   [rows][n] bfloat16 (masked: [G][M_cap][n]), 16-byte aligned, n % 8 == 0
+ * - A K block that runs past k (k % 128 != 0) contributes only its first
+ *   k % 128 columns; the scale of that block still applies.
+ * - Errors found on the host are returned at once (nothing is launched).
+ *   Errors found by the kernel (a wait that exceeded the watchdog limit, a
+ *   group id or count out of range) are recorded in a per-device status word
+ *   and read with fg_get_device_status().
+ */
+#ifndef FP8GEMM_H_
+#define FP8GEMM_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum fg_status {
+    FG_OK = 0,
+    FG_ERR_INVALID_ARG = 1,   /* null pointer, negative or inconsistent size, bad format  */
+    FG_ERR_MISALIGNED = 2,    /* pointer or leading dimension breaks a 16-byte rule        */
+    FG_ERR_UNSUPPORTED = 3,   /* shape outside what the kernels support (e.g. k % 16 != 0) */
+    FG_ERR_CUDA = 4,          /* a CUDA runtime / driver call failed                       */
+    FG_ERR_TIMEOUT = 5,       /* device: a pipeline wait exceeded the watchdog limit       */
+    FG_ERR_DEVICE_CHECK = 6   /* device: group id or masked count out of range             */
+} fg_status;
+
+typedef enum fg_fp8 { FG_E4M3 = 0, FG_E5M2 = 1 } fg_fp8;
+
+/* Dense NT GEMM ("普通密集GEMM"): D[m][n] = A[m][k] x B[n][k]^T with the
+ * fine-grained scales above.  All m x n outputs are written.  m == 0 is a
+ * no-op; n, k >= 1 are required. */
+fg_status fg_gemm_fp8_nt(const void *A, int a_fmt, const float *sA, int ld_sA,
+                         const void *B, int b_fmt, const float *sB,
+                         void *D, int m, int n, int k, void *stream);
+
+/* Contiguous-layout grouped GEMM ("连续布局分组GEMM": groups concatenated on
+ * the M axis, each row tagged with its group).  A is [M][k]; B holds G weight
+ * matrices [G][n][k]; m_indices[r] (int32, device) is the group of row r.
+ * Segments are aligned to 128 rows: within each 128-row tile every row carries
+ * either the group id of the tile's first row or -1 (padding).  Rows whose id
+ * equals the tile's group are written with A[r] x B[g]^T; all other rows of D
+ * are left untouched.  A tile whose first id is outside [0, G) is skipped (and
+ * recorded as FG_ERR_DEVICE_CHECK unless it is -1).  M % 128 == 0. */
+fg_status fg_grouped_gemm_fp8_contiguous(const void *A, int a_fmt, const float *sA, int ld_sA,
+                                         const void *B, int b_fmt, const float *sB, void *D,
+                                         const int32_t *m_indices, int M, int n, int k, int G,
+                                         void *stream);
+
+/* Masked-layout grouped GEMM ("掩码布局分组GEMM": a fixed capacity per group
+ * and a device-side count of valid rows, so the host needs no knowledge of the
+ * counts and the call is CUDA-graph friendly).  A is [G][M_cap][k], sA is
+ * [G][kb][ld_sA], D is [G][M_cap][n]; masked_m[g] (int32, device) rows of group
+ * g are valid.  Rows r < masked_m[g] are written; all other rows are left
+ * untouched.  A count outside [0, M_cap] is clamped into it and recorded as
+ * FG_ERR_DEVICE_CHECK. */
+fg_status fg_grouped_gemm_fp8_masked(const void *A, int a_fmt, const float *sA, int ld_sA,
+                                     const void *B, int b_fmt, const float *sB, void *D,
+                                     const int32_t *masked_m, int G, int M_cap, int n, int k,
+                                     void *stream);
+
+/* Layout helper (the page's "LHS scales must be TMA-aligned and transposed",
+ * section "基本用法"): src is row-major [batches][rows][kb], dst receives
+ * [batches][kb][ld_dst] with ld_dst >= rows, ld_dst % 4 == 0; padding entries
+ * are set to 0.  Device pointers, asynchronous on `stream`. */
+fg_status fg_scales_a_to_mn_major(const float *src, float *dst, int batches, int rows, int kb,
+                                  int ld_dst, void *stream);
+
+/* Smallest valid ld_sA for `rows` rows: rows rounded up to a multiple of 4. */
+int fg_scales_a_ld(int rows);
+
+/* Synchronizes `stream`, then returns and clears the calling device's status
+ * word (FG_OK when no kernel recorded an error).  `detail` (may be NULL)
+ * receives a code saying where: for FG_ERR_TIMEOUT the role (1 producer,
+ * 2 MMA, 3 epilogue) in bits 24..31; for FG_ERR_DEVICE_CHECK the offending
+ * group or tile index. */
+fg_status fg_get_device_status(void *stream, uint32_t *detail);
+
+/* Limit the number of SMs (persistent CTAs) used by later calls on any device
+ * ("SM资源控制"); 0 restores the default (all SMs). */
+fg_status fg_set_num_sms(int num_sms);
+
+/* Watchdog limit of each in-kernel pipeline wait, in milliseconds (default
+ * 2000; 0 restores the default). */
+fg_status fg_set_watchdog_ms(uint32_t ms);
+
+/* Human-readable name of a status code (static storage). */
+const char *fg_status_string(int status);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+int fg_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FP8GEMM_H_ */

@@ -1,0 +1,221 @@
+"""FP8 NT GEMM with fine-grained scaling for GB300 (sm_103a): dense and MoE grouped.
+
+A thin Python binding of the C ABI in ``include/fp8gemm.h``: the functions
+below carry the same names as the C entry points, check and marshal torch
+tensors (device pointers, sizes, the current CUDA stream) and call the
+library through ctypes.  Every step of the computation runs in the library's
+CUDA kernels; there is no other implementation to fall back to, and a
+missing or unloadable library raises.
+
+Layouts (see the header for the full contract):
+  A   [m, k] (masked: [G, M_cap, k]) float8_e4m3fn / float8_e5m2 / uint8
+  sA  MN-major [ceil(k/128), ld] (masked: [G, ceil(k/128), ld]) float32
+  B   [n, k] (grouped: [G, n, k])
+  sB  [ceil(n/128), ceil(k/128)] (grouped: [G, ...]) float32
+  D   [m, n] (masked: [G, M_cap, n]) bfloat16
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import _build
+
+E4M3 = 0
+E5M2 = 1
+
+FG_OK = 0
+STATUS_NAMES = {0: "FG_OK", 1: "FG_ERR_INVALID_ARG", 2: "FG_ERR_MISALIGNED", 3: "FG_ERR_UNSUPPORTED",
+                4: "FG_ERR_CUDA", 5: "FG_ERR_TIMEOUT", 6: "FG_ERR_DEVICE_CHECK"}
+
+_lock = threading.Lock()
+_lib = None
+
+# exported symbols and their ctypes signatures (kept in step with include/fp8gemm.h)
+_P, _I, _U32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_uint32
+SIGNATURES = {
+    "fg_gemm_fp8_nt": (_I, [_P, _I, _P, _I, _P, _I, _P, _P, _I, _I, _I, _P]),
+    "fg_grouped_gemm_fp8_contiguous": (_I, [_P, _I, _P, _I, _P, _I, _P, _P, _P, _I, _I, _I, _I, _P]),
+    "fg_grouped_gemm_fp8_masked": (_I, [_P, _I, _P, _I, _P, _I, _P, _P, _P, _I, _I, _I, _I, _P]),
+    "fg_scales_a_to_mn_major": (_I, [_P, _P, _I, _I, _I, _I, _P]),
+    "fg_scales_a_ld": (_I, [_I]),
+    "fg_get_device_status": (_I, [_P, ctypes.POINTER(_U32)]),
+    "fg_set_num_sms": (_I, [_I]),
+    "fg_set_watchdog_ms": (_I, [_U32]),
+    "fg_status_string": (ctypes.c_char_p, [_I]),
+    "fg_version": (_I, []),
+    "fg_debug_skip_producer_iteration": (_I, [_I]),
+}
+
+
+class FGError(RuntimeError):
+    def __init__(self, fn, status):
+        self.status = status
+        super().__init__(f"{fn} failed: {STATUS_NAMES.get(status, status)}")
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def lib():
+    """The loaded C library (built in-tree on first use if missing)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = _build.build() if os.environ.get("FG_NO_AUTOBUILD") != "1" else _build.LIB_PATH
+            h = ctypes.CDLL(path)
+            for name, (res, args) in SIGNATURES.items():
+                f = getattr(h, name)
+                f.restype = res
+                f.argtypes = args
+            _lib = h
+        return _lib
+
+
+def _check(name, st):
+    if st != FG_OK:
+        raise FGError(name, st)
+
+
+def _stream_ptr(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _fmt_of(t, fmt):
+    if fmt is not None:
+        return int(fmt)
+    if t.dtype == torch.float8_e4m3fn or t.dtype == torch.uint8:
+        return E4M3
+    if t.dtype == torch.float8_e5m2:
+        return E5M2
+    raise TypeError(f"FP8 operand must be float8_e4m3fn, float8_e5m2 or uint8, got {t.dtype}")
+
+
+def _need(t, name, dtypes, dim):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype not in dtypes:
+        raise TypeError(f"{name} has dtype {t.dtype}, expected one of {dtypes}")
+    if t.dim() != dim:
+        raise ValueError(f"{name} must have {dim} dimensions, got shape {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+_FP8 = (torch.float8_e4m3fn, torch.float8_e5m2, torch.uint8)
+_F32 = (torch.float32,)
+_BF16 = (torch.bfloat16,)
+_I32 = (torch.int32,)
+
+
+def _cdiv(a, b):
+    return (a + b - 1) // b
+
+
+def fg_gemm_fp8_nt(A, sA, B, sB, D, *, a_fmt=None, b_fmt=None, stream=None):
+    """Dense D[m,n] = A[m,k] . B[n,k]^T with 1x128 / 128x128 FP32 scales, BF16 out."""
+    _need(A, "A", _FP8, 2), _need(B, "B", _FP8, 2), _need(sA, "sA", _F32, 2)
+    _need(sB, "sB", _F32, 2), _need(D, "D", _BF16, 2)
+    m, k = A.shape
+    n = B.shape[0]
+    if B.shape[1] != k or tuple(D.shape) != (m, n):
+        raise ValueError(f"shape mismatch A{tuple(A.shape)} B{tuple(B.shape)} D{tuple(D.shape)}")
+    if sA.shape[0] != _cdiv(k, 128) or tuple(sB.shape) != (_cdiv(n, 128), _cdiv(k, 128)):
+        raise ValueError(f"scale shapes sA{tuple(sA.shape)} sB{tuple(sB.shape)} do not fit m={m} n={n} k={k}")
+    st = lib().fg_gemm_fp8_nt(A.data_ptr(), _fmt_of(A, a_fmt), sA.data_ptr(), sA.shape[1], B.data_ptr(),
+                              _fmt_of(B, b_fmt), sB.data_ptr(), D.data_ptr(), m, n, k, _stream_ptr(stream))
+    _check("fg_gemm_fp8_nt", st)
+    return D
+
+
+def fg_grouped_gemm_fp8_contiguous(A, sA, B, sB, D, m_indices, *, a_fmt=None, b_fmt=None, stream=None):
+    """Contiguous layout: row r of A multiplies B[m_indices[r]]; rows with -1 stay untouched."""
+    _need(A, "A", _FP8, 2), _need(B, "B", _FP8, 3), _need(sA, "sA", _F32, 2)
+    _need(sB, "sB", _F32, 3), _need(D, "D", _BF16, 2), _need(m_indices, "m_indices", _I32, 1)
+    M, k = A.shape
+    G, n, kb_ = B.shape
+    if kb_ != k or tuple(D.shape) != (M, n) or m_indices.shape[0] != M:
+        raise ValueError("shape mismatch")
+    if sA.shape[0] != _cdiv(k, 128) or tuple(sB.shape) != (G, _cdiv(n, 128), _cdiv(k, 128)):
+        raise ValueError("scale shapes do not fit")
+    st = lib().fg_grouped_gemm_fp8_contiguous(
+        A.data_ptr(), _fmt_of(A, a_fmt), sA.data_ptr(), sA.shape[1], B.data_ptr(), _fmt_of(B, b_fmt),
+        sB.data_ptr(), D.data_ptr(), m_indices.data_ptr(), M, n, k, G, _stream_ptr(stream))
+    _check("fg_grouped_gemm_fp8_contiguous", st)
+    return D
+
+
+def fg_grouped_gemm_fp8_masked(A, sA, B, sB, D, masked_m, *, a_fmt=None, b_fmt=None, stream=None):
+    """Masked layout: rows r < masked_m[g] of group g are written; the rest stay untouched."""
+    _need(A, "A", _FP8, 3), _need(B, "B", _FP8, 3), _need(sA, "sA", _F32, 3)
+    _need(sB, "sB", _F32, 3), _need(D, "D", _BF16, 3), _need(masked_m, "masked_m", _I32, 1)
+    G, M_cap, k = A.shape
+    Gb, n, kb_ = B.shape
+    if Gb != G or kb_ != k or tuple(D.shape) != (G, M_cap, n) or masked_m.shape[0] != G:
+        raise ValueError("shape mismatch")
+    if tuple(sA.shape[:2]) != (G, _cdiv(k, 128)) or tuple(sB.shape) != (G, _cdiv(n, 128), _cdiv(k, 128)):
+        raise ValueError("scale shapes do not fit")
+    st = lib().fg_grouped_gemm_fp8_masked(
+        A.data_ptr(), _fmt_of(A, a_fmt), sA.data_ptr(), sA.shape[2], B.data_ptr(), _fmt_of(B, b_fmt),
+        sB.data_ptr(), D.data_ptr(), masked_m.data_ptr(), G, M_cap, n, k, _stream_ptr(stream))
+    _check("fg_grouped_gemm_fp8_masked", st)
+    return D
+
+
+def fg_scales_a_ld(rows: int) -> int:
+    return lib().fg_scales_a_ld(int(rows))
+
+
+def fg_scales_a_to_mn_major(src, dst=None, *, stream=None):
+    """Row-major [.., rows, kb] FP32 scales -> MN-major [.., kb, ld] (ld = rows rounded up to 4)."""
+    _need(src, "src", _F32, src.dim())
+    if src.dim() not in (2, 3):
+        raise ValueError("src must be [rows, kb] or [batches, rows, kb]")
+    batches = 1 if src.dim() == 2 else src.shape[0]
+    rows, kb = src.shape[-2], src.shape[-1]
+    ld = fg_scales_a_ld(rows)
+    shape = (kb, ld) if src.dim() == 2 else (batches, kb, ld)
+    if dst is None:
+        dst = torch.empty(shape, dtype=torch.float32, device=src.device)
+    else:
+        _need(dst, "dst", _F32, src.dim())
+        if tuple(dst.shape[:-1]) != shape[:-1] or dst.shape[-1] < rows:
+            raise ValueError("dst shape does not fit")
+        ld = dst.shape[-1]
+    st = lib().fg_scales_a_to_mn_major(src.data_ptr(), dst.data_ptr(), batches, rows, kb, ld,
+                                        _stream_ptr(stream))
+    _check("fg_scales_a_to_mn_major", st)
+    return dst
+
+
+def fg_get_device_status(stream=None):
+    """Synchronize the stream; return (status, detail) of this device and clear it."""
+    d = ctypes.c_uint32(0)
+    st = lib().fg_get_device_status(_stream_ptr(stream), ctypes.byref(d))
+    return st, d.value
+
+
+def fg_set_num_sms(n: int) -> None:
+    _check("fg_set_num_sms", lib().fg_set_num_sms(int(n)))
+
+
+def fg_set_watchdog_ms(ms: int) -> None:
+    _check("fg_set_watchdog_ms", lib().fg_set_watchdog_ms(int(ms)))
+
+
+def fg_status_string(st: int) -> str:
+    return lib().fg_status_string(int(st)).decode()
+
+
+def fg_version() -> int:
+    return lib().fg_version()

@@ -1,0 +1,257 @@
+// fp8gemm.cu -- C ABI of the FP8 NT GEMM library (declared in include/fp8gemm.h):
+// argument checks, TMA tensor-map encoding, kernel selection and launch, and the
+// per-device status word written by the kernels' watchdogs and range checks.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cstdint>
+#include <cstdlib>
+#include <mutex>
+
+#include "../../include/fp8gemm.h"
+#include "gemm_kernel.cuh"
+
+namespace {
+
+using fg::GemmParams;
+
+constexpr int kMaxDevices = 64;
+constexpr uint32_t kDefaultWatchdogMs = 2000;
+
+// [0] first error code, [1] detail; one copy per device (module globals are per context)
+__device__ uint32_t g_status[2];
+
+std::atomic<int> g_num_sms_override{0};
+std::atomic<uint32_t> g_watchdog_ms{kDefaultWatchdogMs};
+std::atomic<int> g_debug_skip_iter{-1};
+
+struct DeviceInfo {
+    int num_sms = 0;
+    uint32_t *status = nullptr;
+};
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_dev_mutex;
+
+fg_status cuda_fail() { return FG_ERR_CUDA; }
+
+fg_status device_info(DeviceInfo **out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return cuda_fail();
+    DeviceInfo &d = g_dev[dev];
+    if (d.num_sms == 0) {
+        std::lock_guard<std::mutex> lock(g_dev_mutex);
+        if (d.num_sms == 0) {
+            int sms = 0;
+            void *st = nullptr;
+            if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return cuda_fail();
+            if (cudaGetSymbolAddress(&st, g_status) != cudaSuccess) return cuda_fail();
+            d.status = static_cast<uint32_t *>(st);
+            d.num_sms = sms;
+        }
+    }
+    *out = &d;
+    return FG_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// 2-D tiled tensor map over a row-major [outer][inner] matrix.
+bool encode_2d(CUtensorMap *map, CUtensorMapDataType dt, const void *base, uint64_t inner, uint64_t outer,
+               uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {row_bytes};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t elem_strides[2] = {1, 1};
+    CUresult r = fn(map, dt, 2, const_cast<void *>(base), dims, strides, box, elem_strides,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+int cdiv(int a, int b) { return (a + b - 1) / b; }
+
+template <int BN, int STAGES, int KIND>
+fg_status launch(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &td, const GemmParams &p,
+                 int grid, cudaStream_t stream) {
+    using L = fg::SmemLayout<BN, STAGES>;
+    auto kern = fg::fp8_gemm_kernel<BN, STAGES, KIND>;
+    static std::atomic<uint64_t> configured{0};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const uint64_t bit = 1ull << (dev & 63);
+    if (!(configured.load(std::memory_order_acquire) & bit)) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC_BYTES) !=
+            cudaSuccess)
+            return cuda_fail();
+        configured.fetch_or(bit, std::memory_order_acq_rel);
+    }
+    kern<<<grid, fg::NUM_THREADS, L::ALLOC_BYTES, stream>>>(ta, tb, td, p);
+    return cudaPeekAtLastError() == cudaSuccess ? FG_OK : cuda_fail();
+}
+
+bool fmt_ok(int f) { return f == FG_E4M3 || f == FG_E5M2; }
+
+// Shared part of the three GEMM entry points.
+//   a_rows: rows of the 2-D A / D row space; b_rows: G * n.
+template <int KIND>
+fg_status run(const void *A, int a_fmt, const float *sA, int ld_sA, const void *B, int b_fmt, const float *sB,
+              void *D, const int32_t *m_indices, const int32_t *masked_m, int rows, int G, int n, int k,
+              cudaStream_t stream) {
+    if (!A || !B || !sA || !sB || !D) return FG_ERR_INVALID_ARG;
+    if (!fmt_ok(a_fmt) || !fmt_ok(b_fmt)) return FG_ERR_INVALID_ARG;
+    if (rows < 0 || n < 1 || k < 1 || G < 1) return FG_ERR_INVALID_ARG;
+    if (ld_sA < rows || ld_sA < 1) return FG_ERR_INVALID_ARG;
+    if (KIND == fg::KIND_CONTIGUOUS && !m_indices) return FG_ERR_INVALID_ARG;
+    if (KIND == fg::KIND_MASKED && !masked_m) return FG_ERR_INVALID_ARG;
+    if (k % 16 != 0 || n % 8 != 0) return FG_ERR_UNSUPPORTED;
+    if (KIND == fg::KIND_CONTIGUOUS && rows % fg::BLOCK_M != 0) return FG_ERR_UNSUPPORTED;
+    if (ld_sA % 4 != 0) return FG_ERR_MISALIGNED;
+    if (!aligned16(A) || !aligned16(B) || !aligned16(D) || !aligned4(sA) || !aligned4(sB)) return FG_ERR_MISALIGNED;
+    const long long a_rows_total = (KIND == fg::KIND_MASKED) ? (long long)G * rows : rows;
+    if ((long long)G * n > INT32_MAX || a_rows_total > INT32_MAX) return FG_ERR_UNSUPPORTED;
+    if (rows == 0) return FG_OK;
+
+    DeviceInfo *dev = nullptr;
+    if (fg_status st = device_info(&dev); st != FG_OK) return st;
+
+    constexpr int BN = 256;
+    constexpr int STAGES = 4;
+    CUtensorMap ta, tb, td;
+    if (!encode_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, (uint64_t)k, (uint64_t)a_rows_total, (uint64_t)k,
+                   fg::BLOCK_K, fg::BLOCK_M) ||
+        !encode_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, (uint64_t)k, (uint64_t)G * n, (uint64_t)k, fg::BLOCK_K,
+                   BN) ||
+        !encode_2d(&td, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, D, (uint64_t)n, (uint64_t)a_rows_total,
+                   (uint64_t)n * 2, 64, 32))
+        return cuda_fail();
+
+    GemmParams p{};
+    p.rows = rows;
+    p.n = n;
+    p.k = k;
+    p.num_groups = G;
+    p.num_kb = cdiv(k, fg::BLOCK_K);
+    p.num_nb = cdiv(n, 128);
+    p.num_n_blocks = cdiv(n, BN);
+    p.num_m_blocks = cdiv(rows, fg::BLOCK_M);
+    p.ld_sa = ld_sA;
+    p.idesc = fg::make_idesc_f8f6f4(fg::BLOCK_M, BN, (uint32_t)a_fmt, (uint32_t)b_fmt);
+    p.sA = sA;
+    p.sB = sB;
+    p.m_indices = m_indices;
+    p.masked_m = masked_m;
+    p.D = static_cast<__nv_bfloat16 *>(D);
+    p.status = dev->status;
+    p.timeout_ns = (unsigned long long)g_watchdog_ms.load() * 1000000ull;
+    p.debug_skip_iter = g_debug_skip_iter.exchange(-1);
+
+    const long long max_tiles =
+        (long long)p.num_m_blocks * p.num_n_blocks * (KIND == fg::KIND_MASKED ? G : 1);
+    int sms = dev->num_sms;
+    const int ovr = g_num_sms_override.load();
+    if (ovr > 0 && ovr < sms) sms = ovr;
+    const int grid = (int)(max_tiles < sms ? max_tiles : sms);
+    return launch<BN, STAGES, KIND>(ta, tb, td, p, grid, stream);
+}
+
+}  // namespace
+
+extern "C" {
+
+fg_status fg_gemm_fp8_nt(const void *A, int a_fmt, const float *sA, int ld_sA, const void *B, int b_fmt,
+                         const float *sB, void *D, int m, int n, int k, void *stream) {
+    return run<fg::KIND_DENSE>(A, a_fmt, sA, ld_sA, B, b_fmt, sB, D, nullptr, nullptr, m, 1, n, k,
+                               static_cast<cudaStream_t>(stream));
+}
+
+fg_status fg_grouped_gemm_fp8_contiguous(const void *A, int a_fmt, const float *sA, int ld_sA, const void *B,
+                                         int b_fmt, const float *sB, void *D, const int32_t *m_indices, int M,
+                                         int n, int k, int G, void *stream) {
+    return run<fg::KIND_CONTIGUOUS>(A, a_fmt, sA, ld_sA, B, b_fmt, sB, D, m_indices, nullptr, M, G, n, k,
+                                    static_cast<cudaStream_t>(stream));
+}
+
+fg_status fg_grouped_gemm_fp8_masked(const void *A, int a_fmt, const float *sA, int ld_sA, const void *B,
+                                     int b_fmt, const float *sB, void *D, const int32_t *masked_m, int G,
+                                     int M_cap, int n, int k, void *stream) {
+    return run<fg::KIND_MASKED>(A, a_fmt, sA, ld_sA, B, b_fmt, sB, D, nullptr, masked_m, M_cap, G, n, k,
+                                static_cast<cudaStream_t>(stream));
+}
+
+fg_status fg_scales_a_to_mn_major(const float *src, float *dst, int batches, int rows, int kb, int ld_dst,
+                                  void *stream) {
+    if (!src || !dst || batches < 1 || rows < 0 || kb < 1 || ld_dst < rows || ld_dst < 1) return FG_ERR_INVALID_ARG;
+    if (ld_dst % 4 != 0) return FG_ERR_MISALIGNED;
+    if (kb > 65535 || batches > 65535) return FG_ERR_UNSUPPORTED;
+    dim3 grid((unsigned)cdiv(ld_dst, 256), (unsigned)kb, (unsigned)batches);
+    fg::scales_to_mn_major_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(src, dst, rows, kb, ld_dst);
+    return cudaPeekAtLastError() == cudaSuccess ? FG_OK : FG_ERR_CUDA;
+}
+
+int fg_scales_a_ld(int rows) { return rows <= 0 ? 4 : (rows + 3) / 4 * 4; }
+
+fg_status fg_get_device_status(void *stream, uint32_t *detail) {
+    DeviceInfo *dev = nullptr;
+    if (fg_status st = device_info(&dev); st != FG_OK) return st;
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return FG_ERR_CUDA;
+    uint32_t host[2] = {0, 0};
+    if (cudaMemcpyFromSymbol(host, g_status, sizeof(host)) != cudaSuccess) return FG_ERR_CUDA;
+    const uint32_t zero[2] = {0, 0};
+    if (cudaMemcpyToSymbol(g_status, zero, sizeof(zero)) != cudaSuccess) return FG_ERR_CUDA;
+    if (detail) *detail = host[1];
+    return static_cast<fg_status>(host[0]);
+}
+
+fg_status fg_set_num_sms(int num_sms) {
+    if (num_sms < 0) return FG_ERR_INVALID_ARG;
+    g_num_sms_override.store(num_sms);
+    return FG_OK;
+}
+
+fg_status fg_set_watchdog_ms(uint32_t ms) {
+    g_watchdog_ms.store(ms == 0 ? kDefaultWatchdogMs : ms);
+    return FG_OK;
+}
+
+// Test hook (not part of the public header): in the next GEMM call, the
+// producer of every CTA leaves its K iteration `iter` unarmed, so the MMA
+// warp's bounded wait expires and the call reports FG_ERR_TIMEOUT.
+fg_status fg_debug_skip_producer_iteration(int iter) {
+    g_debug_skip_iter.store(iter);
+    return FG_OK;
+}
+
+const char *fg_status_string(int status) {
+    switch (status) {
+        case FG_OK: return "FG_OK";
+        case FG_ERR_INVALID_ARG: return "FG_ERR_INVALID_ARG";
+        case FG_ERR_MISALIGNED: return "FG_ERR_MISALIGNED";
+        case FG_ERR_UNSUPPORTED: return "FG_ERR_UNSUPPORTED";
+        case FG_ERR_CUDA: return "FG_ERR_CUDA";
+        case FG_ERR_TIMEOUT: return "FG_ERR_TIMEOUT";
+        case FG_ERR_DEVICE_CHECK: return "FG_ERR_DEVICE_CHECK";
+        default: return "FG_ERR_UNKNOWN";
+    }
+}
+
+int fg_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,476 @@
+// gemm_kernel.cuh -- persistent, warp-specialized FP8 NT GEMM for sm_103a with
+// fine-grained scaling and two-level accumulation, for the dense layout and the
+// two MoE grouped layouts (contiguous and masked).
+//
+// Method (page "DeepSeek开源周第三天DeepGEMM"): each 128-wide K block is
+// multiplied on the tensor cores into a fresh FP32 partial, which is then
+// scaled by sA[row, kb] * sB[col/128, kb] and added to an FP32 running sum on
+// the CUDA cores (promotion excerpt "两级精度累加与细粒度缩放"); BF16 output.
+//
+// Blackwell mapping (one CTA per SM, 320 threads):
+//   warp 8      TMA producer: one lane loads the A tile (128 x 128 B) and the
+//               B tile (BN x 128 B) of each K block into a STAGES-deep
+//               shared-memory ring (128-byte swizzle), signalling `full[s]`.
+//   warp 9      MMA issuer: one lane issues 4 tcgen05.mma (K = 32 each) per K
+//               block into one of two TMEM accumulators (128 lanes x BN
+//               columns, FP32), then commits to `empty[s]` (smem stage free)
+//               and `tmem_full[b]` (partial ready).
+//   warps 0..7  promotion + epilogue: warp w reads TMEM lanes 32*(w%4).. (its
+//               rows) and columns [(w/4)*BN/2, (w/4+1)*BN/2) with tcgen05.ld,
+//               multiplies by sA*sB (loaded one K block ahead from global
+//               memory) and adds into BN/2 FP32 registers per thread, then
+//               releases the TMEM buffer (`tmem_empty[b]`).  After the last K
+//               block a warp converts its 32 x BN/2 block to BF16, stages it in
+//               swizzled shared memory and writes it with TMA stores, or with
+//               per-row predicated stores when some of its rows must stay
+//               untouched (grouped layouts).
+// The two TMEM accumulators let the tensor cores run K block kb+1 while the
+// promotion warps consume K block kb, and run the next tile's first K blocks
+// while the epilogue of the previous tile drains.
+//
+// Every wait is bounded by a %globaltimer watchdog: on expiry the kernel
+// records FG_ERR_TIMEOUT in the status word, raises a CTA-wide abort flag,
+// waits (bounded) for its own copies and MMAs in flight, frees TMEM and exits.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cstdint>
+
+#include "ptx.cuh"
+
+namespace fg {
+
+enum : int { KIND_DENSE = 0, KIND_CONTIGUOUS = 1, KIND_MASKED = 2 };
+
+// device-side status codes (same values as fg_status in fp8gemm.h)
+enum : uint32_t { DEV_ERR_TIMEOUT = 5, DEV_ERR_CHECK = 6 };
+enum : uint32_t { ROLE_PRODUCER = 1, ROLE_MMA = 2, ROLE_EPILOGUE = 3 };
+
+constexpr int BLOCK_M = 128;
+constexpr int BLOCK_K = 128;  // K block of the scales and of promotion
+constexpr int MMA_K = 32;     // K of one tcgen05.mma kind::f8f6f4
+constexpr int NUM_EPI_WARPS = 8;
+constexpr int PRODUCER_WARP = 8;
+constexpr int MMA_WARP = 9;
+constexpr int NUM_THREADS = 320;
+constexpr int STAGING_BYTES_PER_WARP = 32 * 128;  // 32 rows x 64 BF16 columns
+constexpr int A_STAGE_BYTES = BLOCK_M * BLOCK_K;
+
+struct GemmParams {
+    int rows;          // rows of the A / D row space: dense m, contiguous M, masked M_cap
+    int n, k;
+    int num_groups;    // G (1 for dense)
+    int num_kb;        // ceil(k / 128)
+    int num_nb;        // ceil(n / 128): rows of sB per group
+    int num_n_blocks;  // ceil(n / BN)
+    int num_m_blocks;  // ceil(rows / 128) (per group for masked)
+    int ld_sa;
+    uint32_t idesc;    // tcgen05 instruction descriptor (formats of A and B)
+    const float *sA;
+    const float *sB;
+    const int32_t *m_indices;
+    const int32_t *masked_m;
+    __nv_bfloat16 *D;
+    uint32_t *status;  // [0] first error code, [1] its detail
+    unsigned long long timeout_ns;
+    int debug_skip_iter;  // producer leaves this K iteration unarmed (-1: never)
+};
+
+template <int BN, int STAGES>
+struct SmemLayout {
+    static constexpr int B_STAGE_BYTES = BN * BLOCK_K;
+    static constexpr int A_OFF = 0;
+    static constexpr int B_OFF = A_OFF + STAGES * A_STAGE_BYTES;
+    static constexpr int STG_OFF = B_OFF + STAGES * B_STAGE_BYTES;
+    static constexpr int BAR_OFF = STG_OFF + NUM_EPI_WARPS * STAGING_BYTES_PER_WARP;
+    static constexpr int NUM_BARS = 2 * STAGES + 4 + 1;  // full, empty, tmem_full x2, tmem_empty x2, drain
+    static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
+    static constexpr int BYTES = MISC_OFF + 16;
+    static constexpr int ALLOC_BYTES = BYTES + 1024;  // slack to align the base to 1024
+    static constexpr int TMEM_COLS = 2 * BN;
+};
+
+__device__ __forceinline__ int clamp_count(int c, int cap) { return c < 0 ? 0 : (c > cap ? cap : c); }
+
+__device__ __forceinline__ void record_error(const GemmParams &p, uint32_t code, uint32_t detail) {
+    if (atomicCAS(p.status, 0u, code) == 0u) atomicExch(p.status + 1, detail);
+}
+
+struct Tile {
+    int valid;
+    int group;
+    int m_blk;      // M block within the group (masked) or within the whole A
+    int n_blk;
+    int a_row;      // first row of the tile in the 2-D row space of A and D
+    int b_row;      // first row of the tile in the 2-D row space of B ([G*n][k])
+    int row_limit;  // rows of the tile below the bound (dense m, masked count)
+};
+
+template <int KIND>
+__device__ __forceinline__ int total_tiles(const GemmParams &p) {
+    if constexpr (KIND == KIND_MASKED) {
+        int mb = 0;
+        for (int g = 0; g < p.num_groups; ++g)
+            mb += (clamp_count(__ldg(p.masked_m + g), p.rows) + BLOCK_M - 1) / BLOCK_M;
+        return mb * p.num_n_blocks;
+    } else {
+        return p.num_m_blocks * p.num_n_blocks;
+    }
+}
+
+// Tile t of the persistent walk: N blocks vary fastest, so the CTAs that run
+// at the same time share their A rows and sweep B together.
+template <int BN, int KIND>
+__device__ __forceinline__ Tile get_tile(const GemmParams &p, int t) {
+    Tile ti;
+    const int mb_lin = t / p.num_n_blocks;
+    ti.n_blk = t - mb_lin * p.num_n_blocks;
+    if constexpr (KIND == KIND_DENSE) {
+        ti.valid = 1;
+        ti.group = 0;
+        ti.m_blk = mb_lin;
+        ti.a_row = mb_lin * BLOCK_M;
+        ti.b_row = ti.n_blk * BN;
+        ti.row_limit = min(BLOCK_M, p.rows - ti.a_row);
+    } else if constexpr (KIND == KIND_CONTIGUOUS) {
+        const int g = __ldg(p.m_indices + (size_t)mb_lin * BLOCK_M);
+        ti.valid = (g >= 0 && g < p.num_groups);
+        ti.group = g;
+        ti.m_blk = mb_lin;
+        ti.a_row = mb_lin * BLOCK_M;
+        ti.b_row = g * p.n + ti.n_blk * BN;
+        ti.row_limit = BLOCK_M;
+    } else {
+        int g = 0, acc = 0, cnt = 0;
+        for (; g < p.num_groups; ++g) {
+            cnt = clamp_count(__ldg(p.masked_m + g), p.rows);
+            const int nb = (cnt + BLOCK_M - 1) / BLOCK_M;
+            if (mb_lin < acc + nb) break;
+            acc += nb;
+        }
+        ti.valid = g < p.num_groups;
+        ti.group = g;
+        ti.m_blk = mb_lin - acc;
+        ti.a_row = g * p.rows + ti.m_blk * BLOCK_M;
+        ti.b_row = g * p.n + ti.n_blk * BN;
+        ti.row_limit = min(BLOCK_M, cnt - ti.m_blk * BLOCK_M);
+    }
+    return ti;
+}
+
+// Bounded wait on an mbarrier phase.  Returns false on watchdog expiry (after
+// recording it and raising the CTA abort flag) or when another role aborted.
+__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile uint32_t *abort_flag,
+                                           const GemmParams &p, uint32_t role) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    uint32_t spins = 0;
+    while (!mbar_try_wait(bar, parity)) {
+        if (*abort_flag) return false;
+        if ((++spins & 31u) == 0u && global_timer_ns() - t0 > p.timeout_ns) {
+            record_error(p, DEV_ERR_TIMEOUT, (role << 24) | (bar & 0xFFFFu));
+            *abort_flag = 1u;
+            return false;
+        }
+    }
+    return true;
+}
+
+// Bounded wait that ignores the abort flag: used after an abort to let copies
+// and MMAs already in flight land before the CTA frees its resources.
+__device__ __forceinline__ bool drain_phase(uint32_t bar, uint32_t parity, uint64_t timeout_ns) {
+    const uint64_t t0 = global_timer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (global_timer_ns() - t0 > timeout_ns) return false;
+    }
+    return true;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
+                 : "memory");
+}
+
+__device__ __forceinline__ void st_global_v4(void *ptr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(ptr), "r"(a), "r"(b), "r"(c), "r"(d)
+                 : "memory");
+}
+
+template <int BN, int STAGES, int KIND>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
+                    const __grid_constant__ CUtensorMap tmap_d, const GemmParams p) {
+    static_assert(BN == 128 || BN == 256, "BN must be 128 or 256");
+    using L = SmemLayout<BN, STAGES>;
+    constexpr int COLS = BN / 2;  // columns per promotion warp
+    constexpr uint32_t STAGE_TX = A_STAGE_BYTES + L::B_STAGE_BYTES;
+
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_u32 = smem_u32(smem_raw);
+    uint8_t *smem = smem_raw + ((1024u - (raw_u32 & 1023u)) & 1023u);
+    const uint32_t sbase = smem_u32(smem);
+
+    const uint32_t bar0 = sbase + L::BAR_OFF;
+    auto full_bar = [&](uint32_t s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](uint32_t s) { return bar0 + 8u * (STAGES + s); };
+    auto tfull_bar = [&](uint32_t b) { return bar0 + 8u * (2 * STAGES + b); };
+    auto tempty_bar = [&](uint32_t b) { return bar0 + 8u * (2 * STAGES + 2 + b); };
+    const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 4);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::MISC_OFF);
+    volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(smem + L::MISC_OFF + 4);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    // ------------------------------------------------------------- set-up
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(tfull_bar(b), 1);
+            mbar_init(tempty_bar(b), NUM_EPI_WARPS);
+        }
+        mbar_init(drain_bar, 1);
+        *abort_flag = 0u;
+        fence_mbarrier_init();
+    }
+    if (warp == MMA_WARP) {
+        tmem_alloc(smem_u32(tmem_slot), L::TMEM_COLS);
+        tmem_relinquish();
+    }
+    if (warp == PRODUCER_WARP && lane == 0) {
+        prefetch_tensormap(&tmap_a);
+        prefetch_tensormap(&tmap_b);
+        prefetch_tensormap(&tmap_d);
+    }
+    if constexpr (KIND == KIND_MASKED) {
+        if (blockIdx.x == 0 && warp == 0) {
+            for (int g = lane; g < p.num_groups; g += 32) {
+                const int c = __ldg(p.masked_m + g);
+                if (c < 0 || c > p.rows) record_error(p, DEV_ERR_CHECK, (uint32_t)g);
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    const int num_tiles = total_tiles<KIND>(p);
+
+    if (warp == PRODUCER_WARP) {
+        // ------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            uint32_t it = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+                const Tile ti = get_tile<BN, KIND>(p, t);
+                if (!ti.valid) continue;
+                for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
+                    const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
+                    if (!wait_phase(empty_bar(s), ph ^ 1u, abort_flag, p, ROLE_PRODUCER)) {
+                        ok = false;
+                        break;
+                    }
+                    if ((int)it == p.debug_skip_iter) continue;
+                    mbar_arrive_expect_tx(full_bar(s), STAGE_TX);
+                    tma_load_2d(sbase + L::A_OFF + s * A_STAGE_BYTES, &tmap_a, full_bar(s), kb * BLOCK_K,
+                                ti.a_row);
+                    tma_load_2d(sbase + L::B_OFF + s * L::B_STAGE_BYTES, &tmap_b, full_bar(s), kb * BLOCK_K,
+                                ti.b_row);
+                }
+            }
+            if (!ok) {
+                // let the loads still in flight land before the CTA exits
+                const uint32_t first = it > (uint32_t)STAGES ? it - STAGES : 0u;
+                for (uint32_t j = first; j < it; ++j) {
+                    if ((int)j == p.debug_skip_iter) continue;
+                    drain_phase(full_bar(j % STAGES), (j / STAGES) & 1u, p.timeout_ns);
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == MMA_WARP) {
+        // -------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            uint32_t it = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+                const Tile ti = get_tile<BN, KIND>(p, t);
+                if (!ti.valid) continue;
+                for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
+                    const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
+                    const uint32_t b = it & 1u, bph = (it >> 1) & 1u;
+                    if (!wait_phase(tempty_bar(b), bph ^ 1u, abort_flag, p, ROLE_MMA) ||
+                        !wait_phase(full_bar(s), ph, abort_flag, p, ROLE_MMA)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t adesc = make_desc_kmajor_sw128(sbase + L::A_OFF + s * A_STAGE_BYTES);
+                    const uint64_t bdesc = make_desc_kmajor_sw128(sbase + L::B_OFF + s * L::B_STAGE_BYTES);
+#pragma unroll
+                    for (int kk = 0; kk < BLOCK_K / MMA_K; ++kk) {
+                        // advance the start address by kk * 32 bytes inside the swizzle atom
+                        const uint64_t koff = (uint64_t)((kk * MMA_K) >> 4);
+                        mma_f8f6f4(tmem_base + b * BN, adesc + koff, bdesc + koff, p.idesc, kk > 0 ? 1u : 0u);
+                    }
+                    mma_commit(empty_bar(s));
+                    mma_commit(tfull_bar(b));
+                }
+            }
+            if (!ok) {
+                // every MMA issued so far must finish before TMEM is freed
+                mma_commit(drain_bar);
+                drain_phase(drain_bar, 0u, p.timeout_ns);
+            }
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------ promotion + epilogue warps
+        const int sub = warp & 3;   // TMEM lane quarter: rows [32*sub, 32*sub+32)
+        const int half = warp >> 2; // column half: [half*COLS, half*COLS+COLS)
+        const int r = sub * 32 + lane;
+        const uint32_t stg = sbase + L::STG_OFF + warp * STAGING_BYTES_PER_WARP;
+        const uint32_t t_lane = (uint32_t)(sub * 32) << 16;
+        uint32_t it = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+            const Tile ti = get_tile<BN, KIND>(p, t);
+            if (!ti.valid) {
+                if (KIND == KIND_CONTIGUOUS && ti.group != -1 && warp == 0 && lane == 0)
+                    record_error(p, DEV_ERR_CHECK, (uint32_t)t);
+                continue;
+            }
+            // which rows of this warp are written
+            bool row_ok;
+            if constexpr (KIND == KIND_CONTIGUOUS)
+                row_ok = __ldg(p.m_indices + ti.a_row + r) == ti.group;
+            else
+                row_ok = r < ti.row_limit;
+            // scale pointers: this thread's row of sA (MN-major), this warp's block row of sB
+            const bool sa_in = (KIND == KIND_CONTIGUOUS) ? true : (r < ti.row_limit);
+            const float *sa_col;
+            if constexpr (KIND == KIND_MASKED)
+                sa_col = p.sA + (size_t)ti.group * p.num_kb * p.ld_sa + (ti.m_blk * BLOCK_M + r);
+            else
+                sa_col = p.sA + (ti.a_row + r);
+            const int col0 = ti.n_blk * BN + half * COLS;
+            const int nb = min(col0 / 128, p.num_nb - 1);
+            const float *sb_row = p.sB + ((size_t)ti.group * p.num_nb + nb) * p.num_kb;
+
+            float acc[COLS];
+#pragma unroll
+            for (int j = 0; j < COLS; ++j) acc[j] = 0.f;
+
+            float sa_cur = sa_in ? __ldg(sa_col) : 0.f;
+            float sb_cur = __ldg(sb_row);
+            for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
+                float sa_nxt = 0.f, sb_nxt = 0.f;
+                if (kb + 1 < p.num_kb) {
+                    sa_nxt = sa_in ? __ldg(sa_col + (size_t)(kb + 1) * p.ld_sa) : 0.f;
+                    sb_nxt = __ldg(sb_row + kb + 1);
+                }
+                const uint32_t b = it & 1u, bph = (it >> 1) & 1u;
+                const bool got = wait_phase(tfull_bar(b), bph, abort_flag, p, ROLE_EPILOGUE);
+                if (!__all_sync(0xffffffffu, got)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const float sc = sa_cur * sb_cur;
+                const uint32_t taddr = tmem_base + t_lane + b * BN + half * COLS;
+#pragma unroll
+                for (int c = 0; c < COLS / 32; ++c) {
+                    uint32_t v[32];
+                    tmem_ld_32x32b_x32(taddr + c * 32, v);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        reg_fence(v[j]);
+                        acc[c * 32 + j] = fmaf(__uint_as_float(v[j]), sc, acc[c * 32 + j]);
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(tempty_bar(b));
+                sa_cur = sa_nxt;
+                sb_cur = sb_nxt;
+            }
+            if (!ok) break;
+
+            // ---------------------------------------------------- epilogue
+            const int d_row = ti.a_row + sub * 32;  // first row of this warp's block in D
+            bool use_tma;
+            if constexpr (KIND == KIND_DENSE)
+                use_tma = true;  // rows past m are clipped by the tensor map bounds
+            else
+                use_tma = __all_sync(0xffffffffu, row_ok);
+            if (use_tma) {
+                const bool rows_in = (KIND != KIND_DENSE) || (sub * 32 < ti.row_limit);
+#pragma unroll
+                for (int bx = 0; bx < COLS / 64; ++bx) {
+                    const int x = col0 + bx * 64;
+                    if (!rows_in || x >= p.n) continue;  // box entirely outside D: nothing to write
+                    if (lane == 0) bulk_wait_group_read<0>();  // staging buffer free again
+                    __syncwarp();
+#pragma unroll
+                    for (int ch = 0; ch < 8; ++ch) {
+                        const float *f = acc + bx * 64 + ch * 8;
+                        const uint32_t off = (uint32_t)lane * 128u + ((uint32_t)(ch ^ (lane & 7)) << 4);
+                        st_shared_v4(stg + off, pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]),
+                                     pack_bf16x2(f[4], f[5]), pack_bf16x2(f[6], f[7]));
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&tmap_d, stg, x, d_row);
+                        bulk_commit_group();
+                    }
+                }
+            } else if (row_ok) {
+                __nv_bfloat16 *drow = p.D + (size_t)(d_row + lane) * p.n;
+#pragma unroll
+                for (int ch = 0; ch < COLS / 8; ++ch) {
+                    const int c = col0 + ch * 8;
+                    if (c < p.n) {
+                        const float *f = acc + ch * 8;
+                        st_global_v4(drow + c, pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]),
+                                     pack_bf16x2(f[4], f[5]), pack_bf16x2(f[6], f[7]));
+                    }
+                }
+            }
+        }
+        if (lane == 0) bulk_wait_group<0>();
+        __syncwarp();
+    }
+
+    // ------------------------------------------------------------ teardown
+    tc_fence_before();
+    __syncthreads();
+    if (warp == MMA_WARP) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, L::TMEM_COLS);
+    }
+}
+
+// Row-major [batches][rows][kb] -> MN-major [batches][kb][ld] (zero padding).
+__global__ void scales_to_mn_major_kernel(const float *__restrict__ src, float *__restrict__ dst, int rows,
+                                          int kb, int ld) {
+    const int r = blockIdx.x * blockDim.x + threadIdx.x;
+    const int j = blockIdx.y;
+    const size_t b = blockIdx.z;
+    if (r >= ld) return;
+    const float v = r < rows ? src[(b * rows + r) * kb + j] : 0.f;
+    dst[(b * kb + j) * ld + r] = v;
+}
+
+}  // namespace fg

@@ -1,0 +1,78 @@
+"""The C ABI library builds, loads without a GPU and exports every function that
+include/fp8gemm.h declares; host-side argument checks return the documented
+status codes before any CUDA call (no compute is launched here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import moe_grouped_gemm_nt_gb300 as fg
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fp8gemm.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(fg_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_three_gemm_calls():
+    names = declared_functions()
+    for n in ("fg_gemm_fp8_nt", "fg_grouped_gemm_fp8_contiguous", "fg_grouped_gemm_fp8_masked"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol():
+    h = ctypes.CDLL(fg._build.build())
+    for name in declared_functions():
+        assert hasattr(h, name), name
+    # the binding knows the signature of every declared function
+    assert set(declared_functions()) <= set(fg.SIGNATURES)
+
+
+def test_host_only_helpers():
+    assert fg.fg_scales_a_ld(1) == 4 and fg.fg_scales_a_ld(4) == 4 and fg.fg_scales_a_ld(130) == 132
+    assert fg.fg_status_string(0) == "FG_OK" and fg.fg_status_string(5) == "FG_ERR_TIMEOUT"
+    assert fg.fg_version() >= 100
+
+
+FAKE = 1 << 20  # a 16-byte aligned fake device address; never dereferenced by these calls
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(A=0), 1),                      # null pointer
+    (dict(a_fmt=3), 1),                  # bad FP8 format
+    (dict(k=24), 3),                     # k % 16 != 0
+    (dict(n=12), 3),                     # n % 8 != 0
+    (dict(ld=130), 2),                   # ld_sA % 4 != 0
+    (dict(ld=64), 1),                    # ld_sA < m
+    (dict(A=FAKE + 8), 2),               # A not 16-byte aligned
+    (dict(D=FAKE + 4), 2),               # D not 16-byte aligned
+    (dict(m=-1), 1),
+    (dict(m=0, ld=4), 0),                # empty problem: a no-op that touches nothing
+])
+def test_dense_argument_checks(kw, expect):
+    a = dict(A=FAKE, a_fmt=0, sA=FAKE, ld=128, B=FAKE, b_fmt=0, sB=FAKE, D=FAKE, m=128, n=256, k=512)
+    a.update(kw)
+    st = fg.lib().fg_gemm_fp8_nt(a["A"], a["a_fmt"], a["sA"], a["ld"], a["B"], a["b_fmt"], a["sB"], a["D"],
+                                 a["m"], a["n"], a["k"], None)
+    assert st == expect
+
+
+def test_grouped_argument_checks():
+    L = fg.lib()
+    # contiguous M must be a multiple of 128; m_indices required
+    assert L.fg_grouped_gemm_fp8_contiguous(FAKE, 0, FAKE, 200, FAKE, 0, FAKE, FAKE, FAKE, 200, 64, 128, 2,
+                                            None) == 3
+    assert L.fg_grouped_gemm_fp8_contiguous(FAKE, 0, FAKE, 256, FAKE, 0, FAKE, FAKE, None, 256, 64, 128, 2,
+                                            None) == 1
+    # masked needs its count tensor and G >= 1
+    assert L.fg_grouped_gemm_fp8_masked(FAKE, 0, FAKE, 256, FAKE, 0, FAKE, FAKE, None, 2, 256, 64, 128,
+                                        None) == 1
+    assert L.fg_grouped_gemm_fp8_masked(FAKE, 0, FAKE, 256, FAKE, 0, FAKE, FAKE, FAKE, 0, 256, 64, 128,
+                                        None) == 1
+    assert L.fg_scales_a_to_mn_major(FAKE, FAKE, 1, 10, 2, 10, None) == 2
+    assert L.fg_scales_a_to_mn_major(FAKE, FAKE, 1, 10, 2, 8, None) == 1
