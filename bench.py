@@ -1,0 +1,424 @@
+"""Benchmark of the FP8 NT GEMM library on its headline workload.
+
+Workload (one step): the dense sweep m in {64, 128, 4096} x (n, k) in
+{(2112,7168), (24576,1536), (7168,16384), (4096,7168), (7168,2048)}: fifteen
+FP8 E4M3 NT GEMMs with 1x128 (LHS) and 128x128 (RHS) FP32 scales and BF16
+output, inputs made from seeded N(0,1) values (scale = amax/448).  Before every
+launch the L2 cache is flushed by writing a 256 MiB buffer; only the GEMM
+launches are inside the CUDA-event intervals that are summed.
+
+Printed: one JSON line on rank 0 with the metric (TFLOP/s over valid FLOPs),
+per-shape TFLOP/s and GB/s, the roofline of the dominant kernel, the
+end-to-end figure (host buffers, copies inside the timed region), the clocks
+seen during the timed region and the CPU oracle as a reported baseline.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+Under torchrun every rank runs the same sweep on its own GPU (independent
+problems, weak scaling); the value is the total work over the slowest rank.
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import io
+import json
+import os
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import workloads as wl  # noqa: E402
+
+METRIC = "FP8 GEMM TFLOPS (valid FLOPs) & HBM GB/s, % of GB300 roofline, 1 GPU"
+UNIT = "TFLOP/s"
+WORKLOAD = ("dense sweep: m in {64,128,4096} x (n,k) in {(2112,7168),(24576,1536),(7168,16384),"
+            "(4096,7168),(7168,2048)}, FP8 E4M3 NT, 1x128/128x128 FP32 scales (amax/448), BF16 out")
+FLUSH_BYTES = 256 << 20
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+FP8_PER_BF16 = 2.0  # nominal dense FP8 / BF16 tensor-core ratio (4.5 / 2.25 PFLOP/s)
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def sweep_problems():
+    """Host problems of the sweep: one seeded m=4096 problem per (n,k); the
+    m = 64 and m = 128 problems are its leading rows."""
+    probs = {}
+    for i, (n, k) in enumerate(wl.DENSE_SWEEP_NK):
+        probs[(n, k)] = wl.dense(max(wl.DENSE_SWEEP_M), n, k, seed=wl.seed_for(1, i))
+    shapes = [(m, n, k) for m in wl.DENSE_SWEEP_M for (n, k) in wl.DENSE_SWEEP_NK]
+    return probs, shapes
+
+
+def problem_bytes(m, n, k):
+    kb, nb = (k + 127) // 128, (n + 127) // 128
+    return m * k + n * k + m * kb * 4 + nb * kb * 4 + m * n * 2
+
+
+# ----------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.dev = device_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(prefix="clocks", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-f", self.path], stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.15)
+        self.proc.terminate()
+        self.proc.wait(timeout=10)
+        rows = []
+        with open(self.path) as f:
+            for r in csv.reader(f):
+                if len(r) >= 9:
+                    rows.append([x.strip() for x in r])
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        pw = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows), "power_w_max": max(pw) if pw else None}
+
+
+# ------------------------------------------------------------ distributed
+
+def dist_setup():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return ws, rank, local
+
+
+def max_over_ranks(x: float, ws: int) -> float:
+    """Largest value of x over all ranks (timing only; no data-path exchange)."""
+    if ws == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ------------------------------------------------------------ CPU oracle
+
+def oracle_sample_rate(probs, shapes, seconds: float, seed: int = 0):
+    """Time the CPU oracle (as it stands) on a bounded sample of the sweep:
+    the same number of random output elements of every problem, sized for
+    about `seconds` of work.  Returns (TFLOP/s of valid work, cores, sample text)."""
+    import oracle
+
+    rng = np.random.default_rng(seed)
+
+    def run(per_shape):
+        flops = 0.0
+        t0 = time.perf_counter()
+        for (m, n, k) in shapes:
+            p = probs[(n, k)]
+            rows = rng.integers(0, m, per_shape)
+            cols = rng.integers(0, n, per_shape)
+            oracle.gemm_fp8_nt_at(p.A[:m], 0, p.sA[:m], p.B, 0, p.sB, rows, cols)
+            flops += 2.0 * k * per_shape
+        return flops, time.perf_counter() - t0
+
+    f0, t0 = run(256)  # calibration
+    per = int(max(64, min(1 << 22, 256 * seconds / max(t0, 1e-6))))
+    f, t = run(per)
+    sample = (f"{per} random output elements of each of the {len(shapes)} sweep problems "
+              f"({f / 2e9:.1f} G MAC, {t:.1f} s)")
+    return f / t / 1e12, oracle.num_threads(), sample
+
+
+# ------------------------------------------------------------------ arms
+
+def run_reference(args, ws, rank):
+    if rank != 0:
+        return
+    probs, shapes = sweep_problems()
+    per_step = max(0.5, min(3.0, 150.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        oracle_sample_rate(probs, shapes, per_step / 4)
+    rates, times = [], []
+    cores, sample = 0, ""
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        r, cores, sample = oracle_sample_rate(probs, shapes, per_step)
+        times.append(time.perf_counter() - t0)
+        rates.append(r)
+    value = float(np.median(rates))
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": float(np.mean(times)) * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "fp8_e4m3",
+        "data": "synthetic (seeded N(0,1), quantized to E4M3)",
+        "config": {"workload": WORKLOAD, "l2": "n/a (CPU)"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, ws, rank, local):
+    import torch
+
+    import moe_grouped_gemm_nt_gb300 as fg
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if args.shapes:
+        # a subset (for profiling): only the problems asked for are generated
+        shapes = [tuple(int(x) for x in s.split(",")) for s in args.shapes.split(";")]
+        probs = {}
+        for (m, n, k) in shapes:
+            idx = wl.DENSE_SWEEP_NK.index((n, k)) if (n, k) in wl.DENSE_SWEEP_NK else 99
+            if (n, k) not in probs or probs[(n, k)].m < m:
+                probs[(n, k)] = wl.dense(m, n, k, seed=wl.seed_for(1, idx))
+    else:
+        probs, shapes = sweep_problems()
+
+    # device copies (inputs resident in HBM before timing)
+    dv = {}
+    for (n, k), p in probs.items():
+        A = torch.from_numpy(p.A).view(torch.float8_e4m3fn).to(dev)
+        B = torch.from_numpy(p.B).view(torch.float8_e4m3fn).to(dev)
+        sA_rm = torch.from_numpy(p.sA).to(dev)
+        sB = torch.from_numpy(p.sB).to(dev)
+        dv[(n, k)] = (A, sA_rm, B, sB)
+    items = []
+    for (m, n, k) in shapes:
+        A, sA_rm, B, sB = dv[(n, k)]
+        sA = fg.fg_scales_a_to_mn_major(sA_rm[:m].contiguous())
+        D = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
+        items.append((m, n, k, A[:m], sA, B, sB, D))
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(record):
+        for i, (m, n, k, A, sA, B, sB, D) in enumerate(items):
+            flush.zero_()
+            e0, e1 = record[i]
+            e0.record(stream)
+            fg.fg_gemm_fp8_nt(A, sA, B, sB, D, stream=stream)
+            e1.record(stream)
+
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in items]
+          for _ in range(args.steps)]
+    warm = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in items]
+    for _ in range(args.warmup):
+        step(warm)
+    torch.cuda.synchronize()
+    st, det = fg.fg_get_device_status()
+    if st != 0:
+        raise RuntimeError(f"device status {st} detail {det:#x} after warm-up")
+
+    clocks = ClockSampler(local)
+    if rank == 0:
+        clocks.start()
+    barrier(ws)
+    torch.cuda.synchronize()
+    w0 = time.perf_counter()
+    for s in range(args.steps):
+        step(ev[s])
+    torch.cuda.synchronize()
+    barrier(ws)
+    wall = time.perf_counter() - w0
+    clock_info = clocks.stop() if rank == 0 else None
+    st, det = fg.fg_get_device_status()
+    if st != 0:
+        raise RuntimeError(f"device status {st} detail {det:#x} after the timed steps")
+
+    per_shape_ms = np.array([[ev[s][i][0].elapsed_time(ev[s][i][1]) for i in range(len(items))]
+                             for s in range(args.steps)])  # [steps, shapes]
+    kernel_ms_per_step = float(per_shape_ms.sum(axis=1).mean())
+    step_ms = max_over_ranks(kernel_ms_per_step, ws)
+    flops_step = sum(2.0 * m * n * k for (m, n, k, *_) in items)
+    bytes_step = sum(problem_bytes(m, n, k) for (m, n, k, *_) in items)
+    value = ws * flops_step / (step_ms * 1e-3) / 1e12
+
+    peaks, peak_src = load_peaks()
+    fp8_peak = peaks["bf16_tflops"] * FP8_PER_BF16
+    hbm_peak = peaks["hbm_gbs"]
+    shape_rows = []
+    med = np.median(per_shape_ms, axis=0)
+    for i, (m, n, k, *_) in enumerate(items):
+        t = med[i] * 1e-3
+        f, b = 2.0 * m * n * k, problem_bytes(m, n, k)
+        t_roof = max(f / (fp8_peak * 1e12), b / (hbm_peak * 1e9))
+        shape_rows.append({"m": m, "n": n, "k": k, "us": round(med[i] * 1e3, 2),
+                           "tflops": round(f / t / 1e12, 1), "gbs": round(b / t / 1e9, 1),
+                           "frac_fp8_peak": round(f / t / 1e12 / fp8_peak, 3),
+                           "frac_hbm_peak": round(b / t / 1e9 / hbm_peak, 3),
+                           "roofline_over_time": round(t_roof / t, 3)})
+    tensor_bound = [r for r in shape_rows if r["m"] >= 4096]
+    hbm_bound = [r for r in shape_rows if r["m"] < 4096]
+
+    def agg(rows, key_work):
+        if not rows:
+            return float("nan")
+        tt = sum(r["us"] for r in rows) * 1e-6
+        if key_work == "flops":
+            return sum(2.0 * r["m"] * r["n"] * r["k"] for r in rows) / tt / 1e12
+        return sum(problem_bytes(r["m"], r["n"], r["k"]) for r in rows) / tt / 1e9
+
+    ach_t = agg(tensor_bound, "flops")
+    ach_h = agg(hbm_bound, "bytes")
+    roofline = {"bound": "tensor", "achieved": round(ach_t, 1), "peak": round(fp8_peak, 1), "unit": "TFLOP/s",
+                "frac": round(ach_t / fp8_peak, 3), "traffic": None,
+                "kernel": "fg::fp8_gemm_kernel<256,4,dense> on the m=4096 shapes",
+                "peak_source": f"{peak_src}: bf16 burst {peaks['bf16_tflops']} x {FP8_PER_BF16} (nominal FP8/BF16)"}
+    roofline_hbm = {"bound": "hbm", "achieved": round(ach_h, 1), "peak": hbm_peak, "unit": "GB/s",
+                    "frac": round(ach_h / hbm_peak, 3), "traffic": None,
+                    "kernel": "fg::fp8_gemm_kernel<256,4,dense> on the m<=128 shapes",
+                    "peak_source": f"{peak_src}: hbm copy"}
+
+    # ------------------------------------------------ end to end (host buffers)
+    e2e = None
+    if not args.no_e2e:
+        host = []
+        for (m, n, k, A, sA, B, sB, D) in items:
+            p = probs[(n, k)]
+            hA = torch.from_numpy(np.ascontiguousarray(p.A[:m])).pin_memory()
+            hsA = torch.from_numpy(np.ascontiguousarray(p.sA[:m])).pin_memory()
+            hB = torch.from_numpy(p.B).pin_memory()
+            hsB = torch.from_numpy(p.sB).pin_memory()
+            hD = torch.empty((m, n), dtype=torch.bfloat16).pin_memory()
+            dA = torch.empty((m, k), dtype=torch.uint8, device=dev)
+            dsA_rm = torch.empty(hsA.shape, dtype=torch.float32, device=dev)
+            dsA = torch.empty(sA.shape, dtype=torch.float32, device=dev)
+            dB = torch.empty(hB.shape, dtype=torch.uint8, device=dev)
+            dsB = torch.empty(hsB.shape, dtype=torch.float32, device=dev)
+            host.append((m, n, k, hA, hsA, hB, hsB, hD, dA, dsA_rm, dsA, dB, dsB, D))
+        h2d = sum(h[3].numel() + h[4].numel() * 4 + h[5].numel() + h[6].numel() * 4 for h in host)
+        d2h = sum(h[7].numel() * 2 for h in host)
+
+        def e2e_step():
+            for (m, n, k, hA, hsA, hB, hsB, hD, dA, dsA_rm, dsA, dB, dsB, D) in host:
+                dA.copy_(hA, non_blocking=True)
+                dsA_rm.copy_(hsA, non_blocking=True)
+                dB.copy_(hB, non_blocking=True)
+                dsB.copy_(hsB, non_blocking=True)
+                fg.fg_scales_a_to_mn_major(dsA_rm, dsA, stream=stream)
+                fg.fg_gemm_fp8_nt(dA, dsA, dB, dsB, D, a_fmt=0, b_fmt=0, stream=stream)
+                hD.copy_(D, non_blocking=True)
+
+        for _ in range(max(1, min(args.warmup, 3))):
+            e2e_step()
+        torch.cuda.synchronize()
+        k_e2e = max(1, min(args.steps, 50))
+        barrier(ws)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(k_e2e):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier(ws)
+        e2e_ms = max_over_ranks(e0.elapsed_time(e1) / k_e2e, ws)
+        e2e = {"value": round(ws * flops_step / (e2e_ms * 1e-3) / 1e12, 2), "unit": UNIT,
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": round(e2e_ms, 3),
+               "steps": k_e2e}
+        st, det = fg.fg_get_device_status()
+        if st != 0:
+            raise RuntimeError(f"device status {st} after the end-to-end steps")
+
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        rate, cores, sample = oracle_sample_rate(probs, shapes, seconds=args.cpu_seconds)
+        cpu = {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(step_ms, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "fp8_e4m3",
+            "data": "synthetic (seeded N(0,1), quantized to E4M3 per 1x128 / 128x128 group)",
+            "config": {"workload": WORKLOAD, "problems_per_step": len(items),
+                       "l2": "flushed before every launch (256 MiB write, outside the timed intervals)",
+                       "timing": "CUDA events around each launch on the launching stream, summed per step",
+                       "parallelism": f"replica x{ws} (independent problems per GPU)"},
+            "hbm_gbs": round(ws * bytes_step / (step_ms * 1e-3) / 1e9, 1),
+            "wall_ms_per_step": round(wall / args.steps * 1e3, 3),
+            "roofline": roofline, "roofline_hbm": roofline_hbm,
+            "shapes": shape_rows, "clocks": clock_info, "e2e": e2e,
+            "gpu_launches": len(items) * args.steps, "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--shapes", default="", help="restrict to 'm,n,k;m,n,k' (profiling)")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    args = ap.parse_args(argv)
+    if args.warmup < 3 and args.impl == "ours" and not args.shapes:
+        ap.error("--warmup must be >= 3")
+    ws, rank, local = dist_setup()
+    try:
+        if args.impl == "reference":
+            run_reference(args, ws, rank)
+        else:
+            run_ours(args, ws, rank, local)
+    finally:
+        if ws > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
