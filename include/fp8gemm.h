@@ -30,9 +30,10 @@
  *     B   [G][n][k] bytes (dense: G = 1)       16-byte aligned
  *     sA  MN-major: [kb][ld_sA] floats, i.e. the scales of K block kb for all
  *         rows are contiguous (masked layout: [G][kb][ld_sA]);
- *         ld_sA >= rows (M_cap for masked), ld_sA % 4 == 0.  Entries past the
- *         rows are never read.  fg_scales_a_to_mn_major() builds this layout
- *         from the row-major [rows][kb] one.
+ *         ld_sA >= rows (M_cap for masked), ld_sA % 4 == 0, sA 16-byte
+ *         aligned (each K block's column is fetched by TMA).  Entries past
+ *         the rows are never used.  fg_scales_a_to_mn_major() builds this
+ *         layout from the row-major [rows][kb] one.
  *     sB  [G][ceil(n/128)][ceil(k/128)] floats, row-major
  *     D   [rows][n] bfloat16 (masked: [G][M_cap][n]), 16-byte aligned, n % 8 == 0
  * - A K block that runs past k (k % 128 != 0) contributes only its first

@@ -69,19 +69,40 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// 2-D tiled tensor map over a row-major [outer][inner] matrix.
-bool encode_2d(CUtensorMap *map, CUtensorMapDataType dt, const void *base, uint64_t inner, uint64_t outer,
-               uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer) {
+// Tiled tensor map (rank 2 or 3) over a row-major array: dims[0] innermost,
+// strides[i] = bytes between consecutive indices of dimension i+1.
+bool encode(CUtensorMap *map, CUtensorMapDataType dt, const void *base, int rank, const uint64_t *dims,
+            const uint64_t *strides, const uint32_t *box, CUtensorMapSwizzle swizzle) {
     auto fn = encode_fn();
     if (!fn) return false;
-    cuuint64_t dims[2] = {inner, outer};
-    cuuint64_t strides[1] = {row_bytes};
-    cuuint32_t box[2] = {box_inner, box_outer};
-    cuuint32_t elem_strides[2] = {1, 1};
-    CUresult r = fn(map, dt, 2, const_cast<void *>(base), dims, strides, box, elem_strides,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    cuuint64_t d[3], st[2];
+    cuuint32_t bx[3], es[3] = {1, 1, 1};
+    for (int i = 0; i < rank; ++i) {
+        d[i] = dims[i];
+        bx[i] = box[i];
+    }
+    for (int i = 0; i + 1 < rank; ++i) st[i] = strides[i];
+    CUresult r = fn(map, dt, (cuuint32_t)rank, const_cast<void *>(base), d, st, bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
+}
+
+bool encode_2d(CUtensorMap *map, CUtensorMapDataType dt, const void *base, uint64_t inner, uint64_t outer,
+               uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer) {
+    const uint64_t dims[2] = {inner, outer};
+    const uint64_t strides[1] = {row_bytes};
+    const uint32_t box[2] = {box_inner, box_outer};
+    return encode(map, dt, base, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+// LHS scales, MN-major: 2-D {rows, kb} with row pitch ld (dense, contiguous) or
+// 3-D {M_cap, kb, G} (masked); each load brings the 128 scales of one K block.
+bool encode_scales_a(CUtensorMap *map, const float *sA, int ld, int rows, int kb, int groups, bool masked) {
+    const uint64_t dims[3] = {(uint64_t)rows, (uint64_t)kb, (uint64_t)groups};
+    const uint64_t strides[2] = {(uint64_t)ld * 4, (uint64_t)ld * 4 * (uint64_t)kb};
+    const uint32_t box[3] = {(uint32_t)fg::BLOCK_M, 1, 1};
+    return encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, sA, masked ? 3 : 2, dims, strides, box,
+                  CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -89,8 +110,8 @@ bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0
 int cdiv(int a, int b) { return (a + b - 1) / b; }
 
 template <int BN, int STAGES, int KIND>
-fg_status launch(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &td, const GemmParams &p,
-                 int grid, cudaStream_t stream) {
+fg_status launch(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &td, const CUtensorMap &tsa,
+                 const GemmParams &p, int grid, cudaStream_t stream) {
     using L = fg::SmemLayout<BN, STAGES>;
     auto kern = fg::fp8_gemm_kernel<BN, STAGES, KIND>;
     static std::atomic<uint64_t> configured{0};
@@ -98,16 +119,28 @@ fg_status launch(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap
     cudaGetDevice(&dev);
     const uint64_t bit = 1ull << (dev & 63);
     if (!(configured.load(std::memory_order_acquire) & bit)) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC_BYTES) !=
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::BYTES) !=
             cudaSuccess)
             return cuda_fail();
         configured.fetch_or(bit, std::memory_order_acq_rel);
     }
-    kern<<<grid, fg::NUM_THREADS, L::ALLOC_BYTES, stream>>>(ta, tb, td, p);
+    kern<<<grid, fg::NUM_THREADS, L::BYTES, stream>>>(ta, tb, td, tsa, p);
     return cudaPeekAtLastError() == cudaSuccess ? FG_OK : cuda_fail();
 }
 
 bool fmt_ok(int f) { return f == FG_E4M3 || f == FG_E5M2; }
+
+// M blocks per raster group: as many as keep the group's A rows (128 x k bytes
+// per block) within about 48 MiB of L2, so B is streamed once per group while
+// A stays resident.  Masked problems walk few M blocks: one group.
+int raster_group_m(int kind, int m_blocks, int k) {
+    if (kind == fg::KIND_MASKED) return m_blocks > 0 ? m_blocks : 1;
+    const long long per_block = (long long)fg::BLOCK_M * k;
+    long long g = (48ll << 20) / (per_block > 0 ? per_block : 1);
+    if (g < 1) g = 1;
+    if (g > m_blocks) g = m_blocks;
+    return (int)(g > 0 ? g : 1);
+}
 
 // Shared part of the three GEMM entry points.
 //   a_rows: rows of the 2-D A / D row space; b_rows: G * n.
@@ -124,7 +157,8 @@ fg_status run(const void *A, int a_fmt, const float *sA, int ld_sA, const void *
     if (k % 16 != 0 || n % 8 != 0) return FG_ERR_UNSUPPORTED;
     if (KIND == fg::KIND_CONTIGUOUS && rows % fg::BLOCK_M != 0) return FG_ERR_UNSUPPORTED;
     if (ld_sA % 4 != 0) return FG_ERR_MISALIGNED;
-    if (!aligned16(A) || !aligned16(B) || !aligned16(D) || !aligned4(sA) || !aligned4(sB)) return FG_ERR_MISALIGNED;
+    if (!aligned16(A) || !aligned16(B) || !aligned16(D) || !aligned16(sA) || !aligned4(sB))
+        return FG_ERR_MISALIGNED;
     const long long a_rows_total = (KIND == fg::KIND_MASKED) ? (long long)G * rows : rows;
     if ((long long)G * n > INT32_MAX || a_rows_total > INT32_MAX) return FG_ERR_UNSUPPORTED;
     if (rows == 0) return FG_OK;
@@ -134,8 +168,9 @@ fg_status run(const void *A, int a_fmt, const float *sA, int ld_sA, const void *
 
     constexpr int BN = 256;
     constexpr int STAGES = 4;
-    CUtensorMap ta, tb, td;
-    if (!encode_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, (uint64_t)k, (uint64_t)a_rows_total, (uint64_t)k,
+    CUtensorMap ta, tb, td, tsa;
+    if (!encode_scales_a(&tsa, sA, ld_sA, rows, cdiv(k, fg::BLOCK_K), G, KIND == fg::KIND_MASKED) ||
+        !encode_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, (uint64_t)k, (uint64_t)a_rows_total, (uint64_t)k,
                    fg::BLOCK_K, fg::BLOCK_M) ||
         !encode_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, (uint64_t)k, (uint64_t)G * n, (uint64_t)k, fg::BLOCK_K,
                    BN) ||
@@ -152,9 +187,8 @@ fg_status run(const void *A, int a_fmt, const float *sA, int ld_sA, const void *
     p.num_nb = cdiv(n, 128);
     p.num_n_blocks = cdiv(n, BN);
     p.num_m_blocks = cdiv(rows, fg::BLOCK_M);
-    p.ld_sa = ld_sA;
+    p.group_m = raster_group_m(KIND, p.num_m_blocks * (KIND == fg::KIND_MASKED ? G : 1), k);
     p.idesc = fg::make_idesc_f8f6f4(fg::BLOCK_M, BN, (uint32_t)a_fmt, (uint32_t)b_fmt);
-    p.sA = sA;
     p.sB = sB;
     p.m_indices = m_indices;
     p.masked_m = masked_m;
@@ -169,7 +203,7 @@ fg_status run(const void *A, int a_fmt, const float *sA, int ld_sA, const void *
     const int ovr = g_num_sms_override.load();
     if (ovr > 0 && ovr < sms) sms = ovr;
     const int grid = (int)(max_tiles < sms ? max_tiles : sms);
-    return launch<BN, STAGES, KIND>(ta, tb, td, p, grid, stream);
+    return launch<BN, STAGES, KIND>(ta, tb, td, tsa, p, grid, stream);
 }
 
 }  // namespace

@@ -8,22 +8,27 @@
 // the CUDA cores (promotion excerpt "两级精度累加与细粒度缩放"); BF16 output.
 //
 // Blackwell mapping (one CTA per SM, 320 threads):
-//   warp 8      TMA producer: one lane loads the A tile (128 x 128 B) and the
-//               B tile (BN x 128 B) of each K block into a STAGES-deep
-//               shared-memory ring (128-byte swizzle), signalling `full[s]`.
+//   warp 8      producer: one lane loads, per K block, the A tile (128 x 128 B)
+//               and the B tile (BN x 128 B) into a STAGES-deep shared-memory
+//               ring (TMA, 128-byte swizzle, `full[s]`), and the block's scales
+//               into a SCALE_STAGES-deep scale ring: the tile's 128 LHS scales
+//               by TMA from the MN-major sA (one 512-byte row, the reason the
+//               layout is MN-major) and the two RHS block scales by cp.async
+//               (`scale_full[q]`).
 //   warp 9      MMA issuer: one lane issues 4 tcgen05.mma (K = 32 each) per K
 //               block into one of two TMEM accumulators (128 lanes x BN
 //               columns, FP32), then commits to `empty[s]` (smem stage free)
 //               and `tmem_full[b]` (partial ready).
-//   warps 0..7  promotion + epilogue: warp w reads TMEM lanes 32*(w%4).. (its
-//               rows) and columns [(w/4)*BN/2, (w/4+1)*BN/2) with tcgen05.ld,
-//               multiplies by sA*sB (loaded one K block ahead from global
-//               memory) and adds into BN/2 FP32 registers per thread, then
-//               releases the TMEM buffer (`tmem_empty[b]`).  After the last K
-//               block a warp converts its 32 x BN/2 block to BF16, stages it in
-//               swizzled shared memory and writes it with TMA stores, or with
-//               per-row predicated stores when some of its rows must stay
-//               untouched (grouped layouts).
+//   warps 0..7  promotion + epilogue: warp w owns TMEM lanes 32*(w%4).. (its
+//               rows) and columns [(w/4)*BN/2, (w/4+1)*BN/2).  Per K block it
+//               reads its scales from the scale ring (releasing the entry), reads
+//               the partial with 32-column tcgen05.ld, hands the TMEM buffer back
+//               (`tmem_empty[b]`) as soon as the last load has landed, and adds
+//               sA*sB*partial into BN/2 FP32 registers per thread with packed
+//               fma.rn.f32x2.  After the last K block a warp converts its
+//               32 x BN/2 block to BF16, stages it in swizzled shared memory and
+//               writes it with TMA stores, or with per-row predicated stores
+//               when some of its rows must stay untouched (grouped layouts).
 // The two TMEM accumulators let the tensor cores run K block kb+1 while the
 // promotion warps consume K block kb, and run the next tile's first K blocks
 // while the epilogue of the previous tile drains.
@@ -44,7 +49,7 @@ enum : int { KIND_DENSE = 0, KIND_CONTIGUOUS = 1, KIND_MASKED = 2 };
 
 // device-side status codes (same values as fg_status in fp8gemm.h)
 enum : uint32_t { DEV_ERR_TIMEOUT = 5, DEV_ERR_CHECK = 6 };
-enum : uint32_t { ROLE_PRODUCER = 1, ROLE_MMA = 2, ROLE_EPILOGUE = 3 };
+enum : uint32_t { ROLE_PRODUCER = 1, ROLE_MMA = 2, ROLE_EPILOGUE = 3, ROLE_SETUP = 4 };
 
 constexpr int BLOCK_M = 128;
 constexpr int BLOCK_K = 128;  // K block of the scales and of promotion
@@ -53,8 +58,12 @@ constexpr int NUM_EPI_WARPS = 8;
 constexpr int PRODUCER_WARP = 8;
 constexpr int MMA_WARP = 9;
 constexpr int NUM_THREADS = 320;
+constexpr int TMEM_LD_COLS = 32;  // columns per promotion TMEM load
 constexpr int STAGING_BYTES_PER_WARP = 32 * 128;  // 32 rows x 64 BF16 columns
 constexpr int A_STAGE_BYTES = BLOCK_M * BLOCK_K;
+constexpr int SA_STAGE_BYTES = BLOCK_M * 4;      // 128 LHS scales of one K block
+constexpr int SB_STAGE_BYTES = 16;               // the RHS scales of the two column halves
+constexpr int SCALE_STAGES = 4;
 
 struct GemmParams {
     int rows;          // rows of the A / D row space: dense m, contiguous M, masked M_cap
@@ -64,9 +73,8 @@ struct GemmParams {
     int num_nb;        // ceil(n / 128): rows of sB per group
     int num_n_blocks;  // ceil(n / BN)
     int num_m_blocks;  // ceil(rows / 128) (per group for masked)
-    int ld_sa;
+    int group_m;       // M blocks per raster group (tiles walk N inside a group of M blocks)
     uint32_t idesc;    // tcgen05 instruction descriptor (formats of A and B)
-    const float *sA;
     const float *sB;
     const int32_t *m_indices;
     const int32_t *masked_m;
@@ -82,11 +90,13 @@ struct SmemLayout {
     static constexpr int A_OFF = 0;
     static constexpr int B_OFF = A_OFF + STAGES * A_STAGE_BYTES;
     static constexpr int STG_OFF = B_OFF + STAGES * B_STAGE_BYTES;
-    static constexpr int BAR_OFF = STG_OFF + NUM_EPI_WARPS * STAGING_BYTES_PER_WARP;
-    static constexpr int NUM_BARS = 2 * STAGES + 4 + 1;  // full, empty, tmem_full x2, tmem_empty x2, drain
+    static constexpr int SA_OFF = STG_OFF + NUM_EPI_WARPS * STAGING_BYTES_PER_WARP;
+    static constexpr int SB_OFF = SA_OFF + SCALE_STAGES * SA_STAGE_BYTES;
+    static constexpr int BAR_OFF = SB_OFF + SCALE_STAGES * SB_STAGE_BYTES;
+    // full, empty, scale_full, scale_empty, tmem_full x2, tmem_empty x2, drain
+    static constexpr int NUM_BARS = 2 * STAGES + 2 * SCALE_STAGES + 4 + 1;
     static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
     static constexpr int BYTES = MISC_OFF + 16;
-    static constexpr int ALLOC_BYTES = BYTES + 1024;  // slack to align the base to 1024
     static constexpr int TMEM_COLS = 2 * BN;
 };
 
@@ -106,25 +116,34 @@ struct Tile {
     int row_limit;  // rows of the tile below the bound (dense m, masked count)
 };
 
+// M blocks of the whole walk (masked: the valid blocks of all groups).
 template <int KIND>
-__device__ __forceinline__ int total_tiles(const GemmParams &p) {
+__device__ __forceinline__ int total_m_blocks(const GemmParams &p) {
     if constexpr (KIND == KIND_MASKED) {
         int mb = 0;
         for (int g = 0; g < p.num_groups; ++g)
             mb += (clamp_count(__ldg(p.masked_m + g), p.rows) + BLOCK_M - 1) / BLOCK_M;
-        return mb * p.num_n_blocks;
+        return mb;
     } else {
-        return p.num_m_blocks * p.num_n_blocks;
+        return p.num_m_blocks;
     }
 }
 
-// Tile t of the persistent walk: N blocks vary fastest, so the CTAs that run
-// at the same time share their A rows and sweep B together.
+// Tile t of the persistent walk (CTA c takes tiles c, c + grid, ...).  The M
+// blocks are cut into raster groups of `group_m`; the tiles of a group walk its
+// N blocks with M varying fastest, so the CTAs running at the same time share
+// the group's A rows (kept in L2) while B streams through once per group.
+// group_m = 1 makes N vary fastest (B kept in L2, A streamed once).
 template <int BN, int KIND>
-__device__ __forceinline__ Tile get_tile(const GemmParams &p, int t) {
+__device__ __forceinline__ Tile get_tile(const GemmParams &p, int t, int mblocks) {
     Tile ti;
-    const int mb_lin = t / p.num_n_blocks;
-    ti.n_blk = t - mb_lin * p.num_n_blocks;
+    const int per_group = p.group_m * p.num_n_blocks;
+    const int grp = t / per_group;
+    const int rem = t - grp * per_group;
+    const int m0 = grp * p.group_m;
+    const int gm = min(p.group_m, mblocks - m0);
+    const int mb_lin = m0 + rem % gm;
+    ti.n_blk = rem / gm;
     if constexpr (KIND == KIND_DENSE) {
         ti.valid = 1;
         ti.group = 0;
@@ -202,37 +221,57 @@ __device__ __forceinline__ void st_global_v4(void *ptr, uint32_t a, uint32_t b, 
                  : "memory");
 }
 
+__device__ __forceinline__ float ld_shared_f32(uint32_t addr) {
+    float v;
+    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+    return v;
+}
+
+// Tensor maps: A [rows][k] u8, B [G*n][k] u8, D [rows][n] bf16 (all 2-D, 128-byte
+// swizzle); SA over the MN-major LHS scales: 2-D {rows, kb} (dense, contiguous)
+// or 3-D {M_cap, kb, G} (masked), fp32, no swizzle, box of 128 rows.
 template <int BN, int STAGES, int KIND>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
-                    const __grid_constant__ CUtensorMap tmap_d, const GemmParams p) {
+                    const __grid_constant__ CUtensorMap tmap_d, const __grid_constant__ CUtensorMap tmap_sa,
+                    const GemmParams p) {
     static_assert(BN == 128 || BN == 256, "BN must be 128 or 256");
     using L = SmemLayout<BN, STAGES>;
     constexpr int COLS = BN / 2;  // columns per promotion warp
     constexpr uint32_t STAGE_TX = A_STAGE_BYTES + L::B_STAGE_BYTES;
 
-    extern __shared__ uint8_t smem_raw[];
-    const uint32_t raw_u32 = smem_u32(smem_raw);
-    uint8_t *smem = smem_raw + ((1024u - (raw_u32 & 1023u)) & 1023u);
+    extern __shared__ __align__(1024) uint8_t smem[];
     const uint32_t sbase = smem_u32(smem);
 
     const uint32_t bar0 = sbase + L::BAR_OFF;
     auto full_bar = [&](uint32_t s) { return bar0 + 8u * s; };
     auto empty_bar = [&](uint32_t s) { return bar0 + 8u * (STAGES + s); };
-    auto tfull_bar = [&](uint32_t b) { return bar0 + 8u * (2 * STAGES + b); };
-    auto tempty_bar = [&](uint32_t b) { return bar0 + 8u * (2 * STAGES + 2 + b); };
-    const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 4);
+    auto sfull_bar = [&](uint32_t q) { return bar0 + 8u * (2 * STAGES + q); };
+    auto sempty_bar = [&](uint32_t q) { return bar0 + 8u * (2 * STAGES + SCALE_STAGES + q); };
+    auto tfull_bar = [&](uint32_t b) { return bar0 + 8u * (2 * STAGES + 2 * SCALE_STAGES + b); };
+    auto tempty_bar = [&](uint32_t b) { return bar0 + 8u * (2 * STAGES + 2 * SCALE_STAGES + 2 + b); };
+    const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 2 * SCALE_STAGES + 4);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::MISC_OFF);
     volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(smem + L::MISC_OFF + 4);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
+    // The 128-byte swizzled TMA tiles need a 1024-byte aligned base.
+    if (sbase & 1023u) {
+        if (threadIdx.x == 0) record_error(p, DEV_ERR_CHECK, (ROLE_SETUP << 24) | (sbase & 0xFFFFu));
+        return;
+    }
+
     // ------------------------------------------------------------- set-up
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(full_bar(s), 1);
             mbar_init(empty_bar(s), 1);
+        }
+        for (int q = 0; q < SCALE_STAGES; ++q) {
+            mbar_init(sfull_bar(q), 2);  // producer's expect_tx arrival + the cp.async arrival
+            mbar_init(sempty_bar(q), NUM_EPI_WARPS);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(tfull_bar(b), 1);
@@ -250,6 +289,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         prefetch_tensormap(&tmap_a);
         prefetch_tensormap(&tmap_b);
         prefetch_tensormap(&tmap_d);
+        prefetch_tensormap(&tmap_sa);
     }
     if constexpr (KIND == KIND_MASKED) {
         if (blockIdx.x == 0 && warp == 0) {
@@ -264,7 +304,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
-    const int num_tiles = total_tiles<KIND>(p);
+    const int m_blocks = total_m_blocks<KIND>(p);
+    const int num_tiles = m_blocks * p.num_n_blocks;
 
     if (warp == PRODUCER_WARP) {
         // ------------------------------------------------------ TMA producer
@@ -272,11 +313,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             uint32_t it = 0;
             bool ok = true;
             for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
-                const Tile ti = get_tile<BN, KIND>(p, t);
+                const Tile ti = get_tile<BN, KIND>(p, t, m_blocks);
                 if (!ti.valid) continue;
+                // RHS block scales of the two column halves of this tile
+                const int nb0 = min((ti.n_blk * BN) / 128, p.num_nb - 1);
+                const int nb1 = min((ti.n_blk * BN + BN / 2) / 128, p.num_nb - 1);
+                const float *sb0 = p.sB + ((size_t)ti.group * p.num_nb + nb0) * p.num_kb;
+                const float *sb1 = p.sB + ((size_t)ti.group * p.num_nb + nb1) * p.num_kb;
                 for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
                     const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
-                    if (!wait_phase(empty_bar(s), ph ^ 1u, abort_flag, p, ROLE_PRODUCER)) {
+                    const uint32_t q = it % SCALE_STAGES, qph = (it / SCALE_STAGES) & 1u;
+                    if (!wait_phase(empty_bar(s), ph ^ 1u, abort_flag, p, ROLE_PRODUCER) ||
+                        !wait_phase(sempty_bar(q), qph ^ 1u, abort_flag, p, ROLE_PRODUCER)) {
                         ok = false;
                         break;
                     }
@@ -286,14 +334,28 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                 ti.a_row);
                     tma_load_2d(sbase + L::B_OFF + s * L::B_STAGE_BYTES, &tmap_b, full_bar(s), kb * BLOCK_K,
                                 ti.b_row);
+                    mbar_arrive_expect_tx(sfull_bar(q), SA_STAGE_BYTES);
+                    if constexpr (KIND == KIND_MASKED)
+                        tma_load_3d(sbase + L::SA_OFF + q * SA_STAGE_BYTES, &tmap_sa, sfull_bar(q),
+                                    ti.m_blk * BLOCK_M, kb, ti.group);
+                    else
+                        tma_load_2d(sbase + L::SA_OFF + q * SA_STAGE_BYTES, &tmap_sa, sfull_bar(q), ti.a_row, kb);
+                    cp_async_4(sbase + L::SB_OFF + q * SB_STAGE_BYTES, sb0 + kb);
+                    cp_async_4(sbase + L::SB_OFF + q * SB_STAGE_BYTES + 4, sb1 + kb);
+                    cp_async_mbar_arrive_noinc(sfull_bar(q));
                 }
             }
             if (!ok) {
-                // let the loads still in flight land before the CTA exits
+                // let the copies still in flight land before the CTA exits
                 const uint32_t first = it > (uint32_t)STAGES ? it - STAGES : 0u;
                 for (uint32_t j = first; j < it; ++j) {
                     if ((int)j == p.debug_skip_iter) continue;
                     drain_phase(full_bar(j % STAGES), (j / STAGES) & 1u, p.timeout_ns);
+                }
+                const uint32_t firstq = it > (uint32_t)SCALE_STAGES ? it - SCALE_STAGES : 0u;
+                for (uint32_t j = firstq; j < it; ++j) {
+                    if ((int)j == p.debug_skip_iter) continue;
+                    drain_phase(sfull_bar(j % SCALE_STAGES), (j / SCALE_STAGES) & 1u, p.timeout_ns);
                 }
             }
         }
@@ -304,7 +366,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             uint32_t it = 0;
             bool ok = true;
             for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
-                const Tile ti = get_tile<BN, KIND>(p, t);
+                const Tile ti = get_tile<BN, KIND>(p, t, m_blocks);
                 if (!ti.valid) continue;
                 for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
                     const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
@@ -334,17 +396,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
         }
         __syncwarp();
-    } else {
+    } else if (warp < NUM_EPI_WARPS) {
         // ------------------------------------------ promotion + epilogue warps
         const int sub = warp & 3;   // TMEM lane quarter: rows [32*sub, 32*sub+32)
         const int half = warp >> 2; // column half: [half*COLS, half*COLS+COLS)
         const int r = sub * 32 + lane;
         const uint32_t stg = sbase + L::STG_OFF + warp * STAGING_BYTES_PER_WARP;
         const uint32_t t_lane = (uint32_t)(sub * 32) << 16;
+        const uint32_t sa_addr = sbase + L::SA_OFF + r * 4;
+        const uint32_t sb_addr = sbase + L::SB_OFF + half * 4;
         uint32_t it = 0;
         bool ok = true;
         for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
-            const Tile ti = get_tile<BN, KIND>(p, t);
+            const Tile ti = get_tile<BN, KIND>(p, t, m_blocks);
             if (!ti.valid) {
                 if (KIND == KIND_CONTIGUOUS && ti.group != -1 && warp == 0 && lane == 0)
                     record_error(p, DEV_ERR_CHECK, (uint32_t)t);
@@ -356,58 +420,53 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 row_ok = __ldg(p.m_indices + ti.a_row + r) == ti.group;
             else
                 row_ok = r < ti.row_limit;
-            // scale pointers: this thread's row of sA (MN-major), this warp's block row of sB
-            const bool sa_in = (KIND == KIND_CONTIGUOUS) ? true : (r < ti.row_limit);
-            const float *sa_col;
-            if constexpr (KIND == KIND_MASKED)
-                sa_col = p.sA + (size_t)ti.group * p.num_kb * p.ld_sa + (ti.m_blk * BLOCK_M + r);
-            else
-                sa_col = p.sA + (ti.a_row + r);
             const int col0 = ti.n_blk * BN + half * COLS;
-            const int nb = min(col0 / 128, p.num_nb - 1);
-            const float *sb_row = p.sB + ((size_t)ti.group * p.num_nb + nb) * p.num_kb;
 
-            float acc[COLS];
+            uint64_t acc2[COLS / 2];  // FP32 running sums, packed in pairs of columns
 #pragma unroll
-            for (int j = 0; j < COLS; ++j) acc[j] = 0.f;
+            for (int j = 0; j < COLS / 2; ++j) acc2[j] = 0ull;
 
-            float sa_cur = sa_in ? __ldg(sa_col) : 0.f;
-            float sb_cur = __ldg(sb_row);
             for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
-                float sa_nxt = 0.f, sb_nxt = 0.f;
-                if (kb + 1 < p.num_kb) {
-                    sa_nxt = sa_in ? __ldg(sa_col + (size_t)(kb + 1) * p.ld_sa) : 0.f;
-                    sb_nxt = __ldg(sb_row + kb + 1);
-                }
                 const uint32_t b = it & 1u, bph = (it >> 1) & 1u;
-                const bool got = wait_phase(tfull_bar(b), bph, abort_flag, p, ROLE_EPILOGUE);
+                const uint32_t q = it % SCALE_STAGES, qph = (it / SCALE_STAGES) & 1u;
+                const bool got = wait_phase(sfull_bar(q), qph, abort_flag, p, ROLE_EPILOGUE) &&
+                                 wait_phase(tfull_bar(b), bph, abort_flag, p, ROLE_EPILOGUE);
                 if (!__all_sync(0xffffffffu, got)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const float sc = sa_cur * sb_cur;
+                const float sc = ld_shared_f32(sa_addr + q * SA_STAGE_BYTES) *
+                                 ld_shared_f32(sb_addr + q * SB_STAGE_BYTES);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(sempty_bar(q));
+                const uint64_t sc2 = pack_f32x2(sc, sc);
                 const uint32_t taddr = tmem_base + t_lane + b * BN + half * COLS;
 #pragma unroll
-                for (int c = 0; c < COLS / 32; ++c) {
-                    uint32_t v[32];
-                    tmem_ld_32x32b_x32(taddr + c * 32, v);
+                for (int c = 0; c < COLS / TMEM_LD_COLS; ++c) {
+                    uint32_t v[TMEM_LD_COLS];
+                    tmem_ld_32x32b_x32(taddr + c * TMEM_LD_COLS, v);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        reg_fence(v[j]);
-                        acc[c * 32 + j] = fmaf(__uint_as_float(v[j]), sc, acc[c * 32 + j]);
+                    for (int j = 0; j < TMEM_LD_COLS; ++j) reg_fence(v[j]);
+                    if (c == COLS / TMEM_LD_COLS - 1) {
+                        // all of this K block's partial is in registers: hand the
+                        // TMEM buffer back to the MMA warp before the last FMAs
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(tempty_bar(b));
                     }
+#pragma unroll
+                    for (int j = 0; j < TMEM_LD_COLS; j += 2)
+                        ffma2(acc2[(c * TMEM_LD_COLS + j) / 2], v[j], v[j + 1], sc2);
                 }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(tempty_bar(b));
-                sa_cur = sa_nxt;
-                sb_cur = sb_nxt;
             }
             if (!ok) break;
 
             // ---------------------------------------------------- epilogue
+            float acc[COLS];
+#pragma unroll
+            for (int j = 0; j < COLS / 2; ++j) unpack_f32x2(acc2[j], acc[2 * j], acc[2 * j + 1]);
             const int d_row = ti.a_row + sub * 32;  // first row of this warp's block in D
             bool use_tma;
             if constexpr (KIND == KIND_DENSE)
