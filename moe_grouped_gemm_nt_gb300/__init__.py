@@ -45,6 +45,7 @@ SIGNATURES = {
     "fg_get_device_status": (_I, [_P, ctypes.POINTER(_U32)]),
     "fg_set_num_sms": (_I, [_I]),
     "fg_set_watchdog_ms": (_I, [_U32]),
+    "fg_set_config_override": (_I, [_I, _I]),
     "fg_status_string": (ctypes.c_char_p, [_I]),
     "fg_version": (_I, []),
     "fg_debug_skip_producer_iteration": (_I, [_I]),
@@ -207,6 +208,11 @@ def fg_get_device_status(stream=None):
 
 def fg_set_num_sms(n: int) -> None:
     _check("fg_set_num_sms", lib().fg_set_num_sms(int(n)))
+
+
+def fg_set_config_override(block_n: int = 0, split_k: int = 0) -> None:
+    """Force the dense tile plan (block_n 128/256, split_k 1..8; 0 = automatic)."""
+    _check("fg_set_config_override", lib().fg_set_config_override(int(block_n), int(split_k)))
 
 
 def fg_set_watchdog_ms(ms: int) -> None:

@@ -109,24 +109,85 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 int cdiv(int a, int b) { return (a + b - 1) / b; }
 
-template <int BN, int STAGES, int KIND>
-fg_status launch(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &td, const CUtensorMap &tsa,
-                 const GemmParams &p, int grid, cudaStream_t stream) {
+std::atomic<int> g_force_bn{0};
+std::atomic<int> g_force_split{0};
+
+template <int BN, int STAGES, int KIND, bool SPLITK>
+struct Kernel {
     using L = fg::SmemLayout<BN, STAGES>;
-    auto kern = fg::fp8_gemm_kernel<BN, STAGES, KIND>;
-    static std::atomic<uint64_t> configured{0};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    const uint64_t bit = 1ull << (dev & 63);
-    if (!(configured.load(std::memory_order_acquire) & bit)) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::BYTES) !=
-            cudaSuccess)
-            return cuda_fail();
-        configured.fetch_or(bit, std::memory_order_acq_rel);
+
+    static cudaLaunchConfig_t config(int grid, int cluster, cudaStream_t stream, cudaLaunchAttribute *at) {
+        cudaLaunchConfig_t cfg{};
+        cfg.gridDim = dim3(grid, 1, 1);
+        cfg.blockDim = dim3(fg::NUM_THREADS, 1, 1);
+        cfg.dynamicSmemBytes = L::BYTES;
+        cfg.stream = stream;
+        at[0].id = cudaLaunchAttributeClusterDimension;
+        at[0].val.clusterDim.x = cluster;
+        at[0].val.clusterDim.y = 1;
+        at[0].val.clusterDim.z = 1;
+        cfg.attrs = at;
+        cfg.numAttrs = 1;
+        return cfg;
     }
-    kern<<<grid, fg::NUM_THREADS, L::BYTES, stream>>>(ta, tb, td, tsa, p);
-    return cudaPeekAtLastError() == cudaSuccess ? FG_OK : cuda_fail();
-}
+
+    // dynamic shared memory attribute, once per device
+    static bool configure() {
+        static std::atomic<uint64_t> configured{0};
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess) return false;
+        const uint64_t bit = 1ull << (dev & 63);
+        if (configured.load(std::memory_order_acquire) & bit) return true;
+        if (cudaFuncSetAttribute(fg::fp8_gemm_kernel<BN, STAGES, KIND, SPLITK>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, L::BYTES) != cudaSuccess)
+            return false;
+        configured.fetch_or(bit, std::memory_order_acq_rel);
+        return true;
+    }
+
+    // clusters of `cluster` CTAs that can be resident at once (one wave)
+    static int max_active_clusters(int cluster) {
+        static std::atomic<int> cache[kMaxDevices][9];
+        int dev = 0;
+        if (cluster < 1 || cluster > 8 || cudaGetDevice(&dev) != cudaSuccess || dev >= kMaxDevices) return 0;
+        const int v = cache[dev][cluster].load();
+        if (v > 0) return v;
+        if (!configure()) return 0;
+        cudaLaunchAttribute at[1];
+        cudaLaunchConfig_t cfg = config(cluster, cluster, nullptr, at);
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, fg::fp8_gemm_kernel<BN, STAGES, KIND, SPLITK>, &cfg) !=
+            cudaSuccess) {
+            cudaGetLastError();
+            return 0;
+        }
+        cache[dev][cluster].store(n);
+        return n;
+    }
+
+    static fg_status launch(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &td,
+                            const CUtensorMap &tsa, const GemmParams &p, int grid, int cluster,
+                            cudaStream_t stream) {
+        if (!configure()) return cuda_fail();
+        if constexpr (!SPLITK) {
+            fg::fp8_gemm_kernel<BN, STAGES, KIND, SPLITK><<<grid, fg::NUM_THREADS, L::BYTES, stream>>>(
+                ta, tb, td, tsa, p);
+        } else {
+            cudaLaunchAttribute at[1];
+            cudaLaunchConfig_t cfg = config(grid, cluster, stream, at);
+            if (cudaLaunchKernelEx(&cfg, fg::fp8_gemm_kernel<BN, STAGES, KIND, SPLITK>, ta, tb, td, tsa, p) !=
+                cudaSuccess)
+                return cuda_fail();
+        }
+        return cudaPeekAtLastError() == cudaSuccess ? FG_OK : cuda_fail();
+    }
+};
+
+// Tile plan of one call: output tile width and split-K factor.
+struct Plan {
+    int bn = 256;
+    int split = 1;  // CTAs per output tile (one cluster); 1 = persistent walk
+};
 
 bool fmt_ok(int f) { return f == FG_E4M3 || f == FG_E5M2; }
 
@@ -166,14 +227,53 @@ fg_status run(const void *A, int a_fmt, const float *sA, int ld_sA, const void *
     DeviceInfo *dev = nullptr;
     if (fg_status st = device_info(&dev); st != FG_OK) return st;
 
-    constexpr int BN = 256;
-    constexpr int STAGES = 4;
+    // ---- plan: persistent 128 x 256 tiles when they fill the GPU; otherwise
+    // (few output tiles, e.g. m <= 128) narrower tiles and/or split-K clusters
+    // so that about one wave of CTAs streams the operands.
+    int sms = dev->num_sms;
+    const int ovr = g_num_sms_override.load();
+    if (ovr > 0 && ovr < sms) sms = ovr;
+    const int num_kb = cdiv(k, fg::BLOCK_K);
+    const long long m_blocks_total = (long long)cdiv(rows, fg::BLOCK_M) * (KIND == fg::KIND_MASKED ? G : 1);
+    Plan plan;
+    if (KIND == fg::KIND_DENSE) {
+        const int fbn = g_force_bn.load(), fsplit = g_force_split.load();
+        if (fbn != 0 || fsplit != 0) {
+            plan.bn = fbn == 128 ? 128 : 256;
+            plan.split = fsplit > 0 ? fsplit : 1;
+        } else {
+            const long long tiles256 = m_blocks_total * cdiv(n, 256);
+            long long best = tiles256 < sms ? tiles256 : sms;
+            if (tiles256 * 4 < (long long)sms * 3) {
+                for (int bn : {256, 128}) {
+                    const long long tiles = m_blocks_total * cdiv(n, bn);
+                    for (int sp = 1; sp <= 8; ++sp) {
+                        if (sp > 1 && num_kb < 2 * sp) break;  // at least two K blocks per rank
+                        long long cap = sms;
+                        if (sp > 1)
+                            cap = (long long)sp * (bn == 256
+                                                       ? Kernel<256, 4, fg::KIND_DENSE, true>::max_active_clusters(sp)
+                                                       : Kernel<128, 6, fg::KIND_DENSE, true>::max_active_clusters(sp));
+                        const long long ctas = tiles * sp;
+                        if (ctas > cap) continue;  // more than one wave
+                        if (ctas > best) {
+                            best = ctas;
+                            plan.bn = bn;
+                            plan.split = sp;
+                        }
+                    }
+                }
+            }
+        }
+    }
+    const int BN = plan.bn;
+
     CUtensorMap ta, tb, td, tsa;
     if (!encode_scales_a(&tsa, sA, ld_sA, rows, cdiv(k, fg::BLOCK_K), G, KIND == fg::KIND_MASKED) ||
         !encode_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, (uint64_t)k, (uint64_t)a_rows_total, (uint64_t)k,
                    fg::BLOCK_K, fg::BLOCK_M) ||
         !encode_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, (uint64_t)k, (uint64_t)G * n, (uint64_t)k, fg::BLOCK_K,
-                   BN) ||
+                   (uint32_t)BN) ||
         !encode_2d(&td, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, D, (uint64_t)n, (uint64_t)a_rows_total,
                    (uint64_t)n * 2, 64, 32))
         return cuda_fail();
@@ -183,7 +283,7 @@ fg_status run(const void *A, int a_fmt, const float *sA, int ld_sA, const void *
     p.n = n;
     p.k = k;
     p.num_groups = G;
-    p.num_kb = cdiv(k, fg::BLOCK_K);
+    p.num_kb = num_kb;
     p.num_nb = cdiv(n, 128);
     p.num_n_blocks = cdiv(n, BN);
     p.num_m_blocks = cdiv(rows, fg::BLOCK_M);
@@ -197,13 +297,23 @@ fg_status run(const void *A, int a_fmt, const float *sA, int ld_sA, const void *
     p.timeout_ns = (unsigned long long)g_watchdog_ms.load() * 1000000ull;
     p.debug_skip_iter = g_debug_skip_iter.exchange(-1);
 
-    const long long max_tiles =
-        (long long)p.num_m_blocks * p.num_n_blocks * (KIND == fg::KIND_MASKED ? G : 1);
-    int sms = dev->num_sms;
-    const int ovr = g_num_sms_override.load();
-    if (ovr > 0 && ovr < sms) sms = ovr;
+    const long long max_tiles = m_blocks_total * p.num_n_blocks;
+    if constexpr (KIND == fg::KIND_DENSE) {
+        if (plan.split > 1) {
+            // one cluster of `split` CTAs per output tile
+            const long long grid = max_tiles * plan.split;
+            if (grid > INT32_MAX) return FG_ERR_UNSUPPORTED;
+            if (BN == 256)
+                return Kernel<256, 4, KIND, true>::launch(ta, tb, td, tsa, p, (int)grid, plan.split, stream);
+            return Kernel<128, 6, KIND, true>::launch(ta, tb, td, tsa, p, (int)grid, plan.split, stream);
+        }
+        if (BN == 128) {
+            const int grid = (int)(max_tiles < sms ? max_tiles : sms);
+            return Kernel<128, 6, KIND, false>::launch(ta, tb, td, tsa, p, grid, 1, stream);
+        }
+    }
     const int grid = (int)(max_tiles < sms ? max_tiles : sms);
-    return launch<BN, STAGES, KIND>(ta, tb, td, tsa, p, grid, stream);
+    return Kernel<256, 4, KIND, false>::launch(ta, tb, td, tsa, p, grid, 1, stream);
 }
 
 }  // namespace
@@ -257,6 +367,14 @@ fg_status fg_get_device_status(void *stream, uint32_t *detail) {
 fg_status fg_set_num_sms(int num_sms) {
     if (num_sms < 0) return FG_ERR_INVALID_ARG;
     g_num_sms_override.store(num_sms);
+    return FG_OK;
+}
+
+fg_status fg_set_config_override(int block_n, int split_k) {
+    if ((block_n != 0 && block_n != 128 && block_n != 256) || split_k < 0 || split_k > 8)
+        return FG_ERR_INVALID_ARG;
+    g_force_bn.store(block_n);
+    g_force_split.store(split_k);
     return FG_OK;
 }
 

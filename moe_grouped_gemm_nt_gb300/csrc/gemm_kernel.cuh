@@ -33,6 +33,13 @@
 // promotion warps consume K block kb, and run the next tile's first K blocks
 // while the epilogue of the previous tile drains.
 //
+// Split-K (SPLITK = true, for problems with fewer output tiles than SMs): the
+// grid is one cluster of S CTAs per output tile; CTA rank q runs K blocks
+// [q*KB/S, (q+1)*KB/S) through the same pipeline, writes its FP32 partial tile
+// into its own shared memory, and after a cluster barrier each rank sums one
+// slice of rows over all S partials through distributed shared memory, in rank
+// order (deterministic), and stores it as BF16.  No global scratch memory.
+//
 // Every wait is bounded by a %globaltimer watchdog: on expiry the kernel
 // records FG_ERR_TIMEOUT in the status word, raises a CTA-wide abort flag,
 // waits (bounded) for its own copies and MMAs in flight, frees TMEM and exits.
@@ -98,6 +105,9 @@ struct SmemLayout {
     static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
     static constexpr int BYTES = MISC_OFF + 16;
     static constexpr int TMEM_COLS = 2 * BN;
+    // split-K partial tile (128 x BN FP32), aliased on the operand ring
+    static constexpr int P_OFF = 0;
+    static_assert(BLOCK_M * BN * 4 <= STG_OFF, "partial tile must fit in the operand ring");
 };
 
 __device__ __forceinline__ int clamp_count(int c, int cap) { return c < 0 ? 0 : (c > cap ? cap : c); }
@@ -230,7 +240,7 @@ __device__ __forceinline__ float ld_shared_f32(uint32_t addr) {
 // Tensor maps: A [rows][k] u8, B [G*n][k] u8, D [rows][n] bf16 (all 2-D, 128-byte
 // swizzle); SA over the MN-major LHS scales: 2-D {rows, kb} (dense, contiguous)
 // or 3-D {M_cap, kb, G} (masked), fp32, no swizzle, box of 128 rows.
-template <int BN, int STAGES, int KIND>
+template <int BN, int STAGES, int KIND, bool SPLITK>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                     const __grid_constant__ CUtensorMap tmap_d, const __grid_constant__ CUtensorMap tmap_sa,
@@ -306,13 +316,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
     const int m_blocks = total_m_blocks<KIND>(p);
     const int num_tiles = m_blocks * p.num_n_blocks;
+    // This CTA's work: persistent tiles t_begin, t_begin + t_step, ... over all
+    // K blocks, or (split-K) the one tile of its cluster over its K range.
+    int t_begin = blockIdx.x, t_step = gridDim.x, kb_begin = 0, kb_end = p.num_kb;
+    uint32_t split = 1, rank = 0;
+    if constexpr (SPLITK) {
+        split = cluster_nctarank();
+        rank = cluster_ctarank();
+        t_begin = blockIdx.x / split;
+        t_step = num_tiles > 0 ? num_tiles : 1;
+        kb_begin = (int)(((long long)p.num_kb * rank) / split);
+        kb_end = (int)(((long long)p.num_kb * (rank + 1)) / split);
+    }
 
     if (warp == PRODUCER_WARP) {
         // ------------------------------------------------------ TMA producer
         if (lane == 0) {
             uint32_t it = 0;
             bool ok = true;
-            for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+            for (int t = t_begin; t < num_tiles && ok; t += t_step) {
                 const Tile ti = get_tile<BN, KIND>(p, t, m_blocks);
                 if (!ti.valid) continue;
                 // RHS block scales of the two column halves of this tile
@@ -320,7 +342,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 const int nb1 = min((ti.n_blk * BN + BN / 2) / 128, p.num_nb - 1);
                 const float *sb0 = p.sB + ((size_t)ti.group * p.num_nb + nb0) * p.num_kb;
                 const float *sb1 = p.sB + ((size_t)ti.group * p.num_nb + nb1) * p.num_kb;
-                for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
+                for (int kb = kb_begin; kb < kb_end; ++kb, ++it) {
                     const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
                     const uint32_t q = it % SCALE_STAGES, qph = (it / SCALE_STAGES) & 1u;
                     if (!wait_phase(empty_bar(s), ph ^ 1u, abort_flag, p, ROLE_PRODUCER) ||
@@ -365,10 +387,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (lane == 0) {
             uint32_t it = 0;
             bool ok = true;
-            for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+            for (int t = t_begin; t < num_tiles && ok; t += t_step) {
                 const Tile ti = get_tile<BN, KIND>(p, t, m_blocks);
                 if (!ti.valid) continue;
-                for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
+                for (int kb = kb_begin; kb < kb_end; ++kb, ++it) {
                     const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
                     const uint32_t b = it & 1u, bph = (it >> 1) & 1u;
                     if (!wait_phase(tempty_bar(b), bph ^ 1u, abort_flag, p, ROLE_MMA) ||
@@ -407,7 +429,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const uint32_t sb_addr = sbase + L::SB_OFF + half * 4;
         uint32_t it = 0;
         bool ok = true;
-        for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+        for (int t = t_begin; t < num_tiles && ok; t += t_step) {
             const Tile ti = get_tile<BN, KIND>(p, t, m_blocks);
             if (!ti.valid) {
                 if (KIND == KIND_CONTIGUOUS && ti.group != -1 && warp == 0 && lane == 0)
@@ -426,7 +448,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
             for (int j = 0; j < COLS / 2; ++j) acc2[j] = 0ull;
 
-            for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
+            for (int kb = kb_begin; kb < kb_end; ++kb, ++it) {
                 const uint32_t b = it & 1u, bph = (it >> 1) & 1u;
                 const uint32_t q = it % SCALE_STAGES, qph = (it / SCALE_STAGES) & 1u;
                 const bool got = wait_phase(sfull_bar(q), qph, abort_flag, p, ROLE_EPILOGUE) &&
@@ -445,7 +467,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
                 for (int c = 0; c < COLS / TMEM_LD_COLS; ++c) {
                     uint32_t v[TMEM_LD_COLS];
-                    tmem_ld_32x32b_x32(taddr + c * TMEM_LD_COLS, v);
+                    tmem_ld_32x32b_x16(taddr + c * TMEM_LD_COLS, *reinterpret_cast<uint32_t(*)[16]>(&v[0]));
+                    tmem_ld_32x32b_x16(taddr + c * TMEM_LD_COLS + 16, *reinterpret_cast<uint32_t(*)[16]>(&v[16]));
                     tmem_ld_wait();
 #pragma unroll
                     for (int j = 0; j < TMEM_LD_COLS; ++j) reg_fence(v[j]);
@@ -462,6 +485,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
             }
             if (!ok) break;
+
+            if constexpr (SPLITK) {
+                if (split > 1) {
+                    // partial tile -> own shared memory (the operand ring is idle
+                    // now: every MMA that read it has completed), rows of BN FP32
+                    // with the 16-byte chunks of row r rotated by (r & 7)
+                    const uint32_t prow = sbase + L::P_OFF + (uint32_t)r * (BN * 4);
+#pragma unroll
+                    for (int ch = 0; ch < COLS / 4; ++ch) {
+                        const int cg = half * (COLS / 4) + ch;  // chunk index within the row
+                        float x0, x1, x2, x3;
+                        unpack_f32x2(acc2[2 * ch], x0, x1);
+                        unpack_f32x2(acc2[2 * ch + 1], x2, x3);
+                        st_shared_v4(prow + (uint32_t)((cg ^ (r & 7)) << 4), __float_as_uint(x0),
+                                     __float_as_uint(x1), __float_as_uint(x2), __float_as_uint(x3));
+                    }
+                    continue;  // the cluster reduction below writes D
+                }
+            }
 
             // ---------------------------------------------------- epilogue
             float acc[COLS];
@@ -510,6 +552,48 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         if (lane == 0) bulk_wait_group<0>();
         __syncwarp();
+    }
+
+    if constexpr (SPLITK) {
+        if (split > 1) {
+            // every CTA of the cluster takes both barriers, whatever happened above
+            cluster_sync();
+            const bool tile_ok = t_begin < num_tiles && !*abort_flag;
+            if (tile_ok && warp < NUM_EPI_WARPS) {
+                const Tile ti = get_tile<BN, KIND>(p, t_begin, m_blocks);
+                if (ti.valid) {
+                    constexpr int CH = BN / 4;  // 16-byte chunks per partial row
+                    const int r0 = (int)((BLOCK_M * rank) / split), r1 = (int)((BLOCK_M * (rank + 1)) / split);
+                    const int col_base = ti.n_blk * BN;
+                    for (int item = threadIdx.x; item < (r1 - r0) * CH; item += NUM_EPI_WARPS * 32) {
+                        const int row = r0 + item / CH;
+                        const int ch = item % CH;
+                        const int col = col_base + ch * 4;
+                        bool row_ok;
+                        if constexpr (KIND == KIND_CONTIGUOUS)
+                            row_ok = __ldg(p.m_indices + ti.a_row + row) == ti.group;
+                        else
+                            row_ok = row < ti.row_limit;
+                        if (!row_ok || col >= p.n) continue;
+                        const uint32_t local =
+                            sbase + L::P_OFF + (uint32_t)row * (BN * 4) + (uint32_t)((ch ^ (row & 7)) << 4);
+                        float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
+                        for (uint32_t q = 0; q < split; ++q) {  // fixed rank (= K) order
+                            const float4 v = ld_shared_cluster_v4(map_shared_rank(local, q));
+                            sum.x += v.x;
+                            sum.y += v.y;
+                            sum.z += v.z;
+                            sum.w += v.w;
+                        }
+                        uint2 w;
+                        w.x = pack_bf16x2(sum.x, sum.y);
+                        w.y = pack_bf16x2(sum.z, sum.w);
+                        *reinterpret_cast<uint2 *>(p.D + (size_t)(ti.a_row + row) * p.n + col) = w;
+                    }
+                }
+            }
+            cluster_sync();  // peers may still be reading this CTA's partial until here
+        }
     }
 
     // ------------------------------------------------------------ teardown

@@ -134,3 +134,36 @@ def test_repeatable_bitwise():
     a = d_to_bits(run_dense(p))
     for _ in range(5):
         assert np.array_equal(a, d_to_bits(run_dense(p)))
+
+
+@pytest.fixture
+def plan_override():
+    import moe_grouped_gemm_nt_gb300 as fg
+
+    yield fg.fg_set_config_override
+    fg.fg_set_config_override(0, 0)
+
+
+@pytest.mark.parametrize("bn,split", [(256, 1), (128, 1), (256, 2), (256, 3), (128, 4), (128, 5), (256, 8),
+                                      (128, 8)])
+@pytest.mark.parametrize("m,n,k", [(130, 520, 1280), (64, 2112, 1024), (1, 264, 400)])
+def test_forced_plans_match_oracle(plan_override, bn, split, m, n, k):
+    """Every tile plan (tile width x split-K cluster size, including ranks with
+    no K blocks when split > K blocks) gives the oracle's result."""
+    plan_override(bn, split)
+    p = wl.dense(m, n, k, seed=7000 + m + n + k)
+    _full_check(p, f"dense {m}x{n}x{k} bn={bn} split={split}")
+
+
+def test_split_plans_agree_and_repeat(plan_override):
+    """Split-K reduces in a fixed rank order: repeated calls are bitwise equal."""
+    p = wl.dense(128, 4096, 7168, seed=71)
+    plan_override(128, 4)
+    a = d_to_bits(run_dense(p))
+    for _ in range(3):
+        assert np.array_equal(a, d_to_bits(run_dense(p)))
+    plan_override(256, 1)
+    b = d_to_bits(run_dense(p))
+    ref16, _ = oracle.gemm_fp8_nt(p.A, 0, p.sA, p.B, 0, p.sB, want_f64=False)
+    compare(a, ref16, what="split 4")
+    compare(b, ref16, what="persistent")
