@@ -563,32 +563,56 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 const Tile ti = get_tile<BN, KIND>(p, t_begin, m_blocks);
                 if (ti.valid) {
                     constexpr int CH = BN / 4;  // 16-byte chunks per partial row
+                    constexpr int MAX_SPLIT = 8;
+                    constexpr int STRIDE = NUM_EPI_WARPS * 32;
                     const int r0 = (int)((BLOCK_M * rank) / split), r1 = (int)((BLOCK_M * (rank + 1)) / split);
                     const int col_base = ti.n_blk * BN;
-                    for (int item = threadIdx.x; item < (r1 - r0) * CH; item += NUM_EPI_WARPS * 32) {
-                        const int row = r0 + item / CH;
-                        const int ch = item % CH;
-                        const int col = col_base + ch * 4;
-                        bool row_ok;
-                        if constexpr (KIND == KIND_CONTIGUOUS)
-                            row_ok = __ldg(p.m_indices + ti.a_row + row) == ti.group;
-                        else
-                            row_ok = row < ti.row_limit;
-                        if (!row_ok || col >= p.n) continue;
-                        const uint32_t local =
-                            sbase + L::P_OFF + (uint32_t)row * (BN * 4) + (uint32_t)((ch ^ (row & 7)) << 4);
-                        float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
-                        for (uint32_t q = 0; q < split; ++q) {  // fixed rank (= K) order
-                            const float4 v = ld_shared_cluster_v4(map_shared_rank(local, q));
-                            sum.x += v.x;
-                            sum.y += v.y;
-                            sum.z += v.z;
-                            sum.w += v.w;
+                    const int items = (r1 - r0) * CH;
+                    // two chunks per thread per pass, all ranks' loads issued before any
+                    // use so the distributed-shared-memory latency is paid once per pass
+                    for (int base = threadIdx.x; base < items; base += 2 * STRIDE) {
+                        float4 v[2][MAX_SPLIT];
+                        bool live[2];
+                        int row[2], col[2];
+#pragma unroll
+                        for (int u = 0; u < 2; ++u) {
+                            const int item = base + u * STRIDE;
+                            row[u] = r0 + item / CH;
+                            const int ch = item % CH;
+                            col[u] = col_base + ch * 4;
+                            bool ok_row;
+                            if (item >= items) {
+                                ok_row = false;
+                            } else if constexpr (KIND == KIND_CONTIGUOUS) {
+                                ok_row = __ldg(p.m_indices + ti.a_row + row[u]) == ti.group;
+                            } else {
+                                ok_row = row[u] < ti.row_limit;
+                            }
+                            live[u] = ok_row && col[u] < p.n;
+                            const uint32_t local = sbase + L::P_OFF + (uint32_t)row[u] * (BN * 4) +
+                                                   (uint32_t)((ch ^ (row[u] & 7)) << 4);
+#pragma unroll
+                            for (int q = 0; q < MAX_SPLIT; ++q)
+                                if (live[u] && q < (int)split) v[u][q] = ld_shared_cluster_v4(map_shared_rank(local, q));
                         }
-                        uint2 w;
-                        w.x = pack_bf16x2(sum.x, sum.y);
-                        w.y = pack_bf16x2(sum.z, sum.w);
-                        *reinterpret_cast<uint2 *>(p.D + (size_t)(ti.a_row + row) * p.n + col) = w;
+#pragma unroll
+                        for (int u = 0; u < 2; ++u) {
+                            if (!live[u]) continue;
+                            float4 sum = v[u][0];
+#pragma unroll
+                            for (int q = 1; q < MAX_SPLIT; ++q) {  // fixed rank (= K) order
+                                if (q < (int)split) {
+                                    sum.x += v[u][q].x;
+                                    sum.y += v[u][q].y;
+                                    sum.z += v[u][q].z;
+                                    sum.w += v[u][q].w;
+                                }
+                            }
+                            uint2 w;
+                            w.x = pack_bf16x2(sum.x, sum.y);
+                            w.y = pack_bf16x2(sum.z, sum.w);
+                            *reinterpret_cast<uint2 *>(p.D + (size_t)(ti.a_row + row[u]) * p.n + col[u]) = w;
+                        }
                     }
                 }
             }
