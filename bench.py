@@ -3,9 +3,10 @@
 Workload (one step): the dense sweep m in {64, 128, 4096} x (n, k) in
 {(2112,7168), (24576,1536), (7168,16384), (4096,7168), (7168,2048)}: fifteen
 FP8 E4M3 NT GEMMs with 1x128 (LHS) and 128x128 (RHS) FP32 scales and BF16
-output, inputs made from seeded N(0,1) values (scale = amax/448).  Before every
-launch the L2 cache is flushed by writing a 256 MiB buffer; only the GEMM
-launches are inside the CUDA-event intervals that are summed.
+output, inputs made from seeded N(0,1) values (scale = amax/448).  Every
+problem rotates over identical copies of its inputs and output that together
+exceed twice the L2 cache, so no launch finds its inputs in L2; the K launches
+of a problem run back to back between one pair of CUDA events.
 
 Printed: one JSON line on rank 0 with the metric (TFLOP/s over valid FLOPs),
 per-shape TFLOP/s and GB/s, the roofline of the dominant kernel, the
@@ -40,7 +41,7 @@ METRIC = "FP8 GEMM TFLOPS (valid FLOPs) & HBM GB/s, % of GB300 roofline, 1 GPU"
 UNIT = "TFLOP/s"
 WORKLOAD = ("dense sweep: m in {64,128,4096} x (n,k) in {(2112,7168),(24576,1536),(7168,16384),"
             "(4096,7168),(7168,2048)}, FP8 E4M3 NT, 1x128/128x128 FP32 scales (amax/448), BF16 out")
-FLUSH_BYTES = 256 << 20
+ROTATE_BYTES = 272 << 20  # > 2 x the 129 MB L2 of a GB300
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 FP8_PER_BF16 = 2.0  # nominal dense FP8 / BF16 tensor-core ratio (4.5 / 2.25 PFLOP/s)
 
@@ -63,6 +64,38 @@ def sweep_problems():
         probs[(n, k)] = wl.dense(max(wl.DENSE_SWEEP_M), n, k, seed=wl.seed_for(1, i))
     shapes = [(m, n, k) for m in wl.DENSE_SWEEP_M for (n, k) in wl.DENSE_SWEEP_NK]
     return probs, shapes
+
+
+def kernel_name(block_n, split):
+    stages = 4 if block_n == 256 else 6
+    return f"fg::fp8_gemm_kernel<{block_n},{stages},dense,{'splitk' if split > 1 else 'persistent'}>"
+
+
+def kernel_sources_digest():
+    """Digest of the CUDA sources: DRAM traffic figures are only used when
+    they were captured on the kernels built from these exact sources."""
+    import hashlib
+    h = hashlib.sha1()
+    d = os.path.join(ROOT, "moe_grouped_gemm_nt_gb300", "csrc")
+    for f in sorted(os.listdir(d)):
+        with open(os.path.join(d, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def load_traffic():
+    """{(m, n, k): DRAM bytes per launch} from profiles/dram_traffic.txt lines
+    '<digest> <m> <n> <k> <read+write bytes>' of the current sources."""
+    out = {}
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    if not os.path.exists(path):
+        return out
+    dig = kernel_sources_digest()
+    for line in open(path):
+        f = line.split()
+        if len(f) == 5 and not line.startswith("#") and f[0] == dig:
+            out[(int(f[1]), int(f[2]), int(f[3]))] = float(f[4])
+    return out
 
 
 def problem_bytes(m, n, k):
@@ -234,41 +267,47 @@ def run_ours(args, ws, rank, local):
         sA_rm = torch.from_numpy(p.sA).to(dev)
         sB = torch.from_numpy(p.sB).to(dev)
         dv[(n, k)] = (A, sA_rm, B, sB)
+    # Each problem rotates over identical copies of its inputs and output whose
+    # total size is at least twice the L2 cache, so no launch finds its inputs
+    # in L2; launches of one problem run back to back between one pair of
+    # CUDA events (single-launch event intervals are too coarse for the
+    # microsecond-scale small-m launches).
     items = []
     for (m, n, k) in shapes:
         A, sA_rm, B, sB = dv[(n, k)]
         sA = fg.fg_scales_a_to_mn_major(sA_rm[:m].contiguous())
-        D = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
-        items.append((m, n, k, A[:m], sA, B, sB, D))
-    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+        nbytes = problem_bytes(m, n, k)
+        ncopy = max(2, -(-ROTATE_BYTES // nbytes))
+        copies = [(A[:m].clone(), sA.clone(), B.clone(), sB.clone(),
+                   torch.empty((m, n), dtype=torch.bfloat16, device=dev)) for _ in range(ncopy)]
+        items.append((m, n, k, copies))
+    del dv
     stream = torch.cuda.current_stream()
 
-    def step(record):
-        for i, (m, n, k, A, sA, B, sB, D) in enumerate(items):
-            flush.zero_()
-            e0, e1 = record[i]
-            e0.record(stream)
+    def run_problem(i, reps, start=0):
+        copies = items[i][3]
+        for r in range(reps):
+            A, sA, B, sB, D = copies[(start + r) % len(copies)]
             fg.fg_gemm_fp8_nt(A, sA, B, sB, D, stream=stream)
-            e1.record(stream)
 
-    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in items]
-          for _ in range(args.steps)]
-    warm = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in items]
-    for _ in range(args.warmup):
-        step(warm)
+    for i in range(len(items)):  # warm-up: W passes over every problem
+        run_problem(i, args.warmup * len(items[i][3]))
     torch.cuda.synchronize()
     st, det = fg.fg_get_device_status()
     if st != 0:
         raise RuntimeError(f"device status {st} detail {det:#x} after warm-up")
 
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in items]
     clocks = ClockSampler(local)
     if rank == 0:
         clocks.start()
     barrier(ws)
     torch.cuda.synchronize()
     w0 = time.perf_counter()
-    for s in range(args.steps):
-        step(ev[s])
+    for i in range(len(items)):  # K steps: K launches of every problem
+        ev[i][0].record(stream)
+        run_problem(i, args.steps)
+        ev[i][1].record(stream)
     torch.cuda.synchronize()
     barrier(ws)
     wall = time.perf_counter() - w0
@@ -277,9 +316,8 @@ def run_ours(args, ws, rank, local):
     if st != 0:
         raise RuntimeError(f"device status {st} detail {det:#x} after the timed steps")
 
-    per_shape_ms = np.array([[ev[s][i][0].elapsed_time(ev[s][i][1]) for i in range(len(items))]
-                             for s in range(args.steps)])  # [steps, shapes]
-    kernel_ms_per_step = float(per_shape_ms.sum(axis=1).mean())
+    per_shape_ms = np.array([ev[i][0].elapsed_time(ev[i][1]) / args.steps for i in range(len(items))])
+    kernel_ms_per_step = float(per_shape_ms.sum())
     step_ms = max_over_ranks(kernel_ms_per_step, ws)
     flops_step = sum(2.0 * m * n * k for (m, n, k, *_) in items)
     bytes_step = sum(problem_bytes(m, n, k) for (m, n, k, *_) in items)
@@ -289,7 +327,7 @@ def run_ours(args, ws, rank, local):
     fp8_peak = peaks["bf16_tflops"] * FP8_PER_BF16
     hbm_peak = peaks["hbm_gbs"]
     shape_rows = []
-    med = np.median(per_shape_ms, axis=0)
+    med = per_shape_ms
     for i, (m, n, k, *_) in enumerate(items):
         t = med[i] * 1e-3
         f, b = 2.0 * m * n * k, problem_bytes(m, n, k)
@@ -299,33 +337,55 @@ def run_ours(args, ws, rank, local):
                            "frac_fp8_peak": round(f / t / 1e12 / fp8_peak, 3),
                            "frac_hbm_peak": round(b / t / 1e9 / hbm_peak, 3),
                            "roofline_over_time": round(t_roof / t, 3)})
-    tensor_bound = [r for r in shape_rows if r["m"] >= 4096]
-    hbm_bound = [r for r in shape_rows if r["m"] < 4096]
+    # group the launches by the kernel instantiation the library's plan picks
+    kern_rows = {}
+    for r in shape_rows:
+        bn, split = fg.fg_query_dense_plan(r["m"], r["n"], r["k"])
+        r["plan"] = {"block_n": bn, "split_k": split}
+        name = kernel_name(bn, split)
+        r["kernel"] = name
+        kern_rows.setdefault(name, []).append(r)
+    traffic_tab = load_traffic()
+    ridge = fp8_peak * 1e12 / (hbm_peak * 1e9)
 
-    def agg(rows, key_work):
-        if not rows:
-            return float("nan")
+    def roof(name, rows):
         tt = sum(r["us"] for r in rows) * 1e-6
-        if key_work == "flops":
-            return sum(2.0 * r["m"] * r["n"] * r["k"] for r in rows) / tt / 1e12
-        return sum(problem_bytes(r["m"], r["n"], r["k"]) for r in rows) / tt / 1e9
+        flops = sum(2.0 * r["m"] * r["n"] * r["k"] for r in rows)
+        byts = sum(problem_bytes(r["m"], r["n"], r["k"]) for r in rows)
+        known = [traffic_tab.get((r["m"], r["n"], r["k"])) for r in rows]
+        traffic = (sum(known) / len(known)) if known and all(v is not None for v in known) else None
+        if flops / byts >= ridge:
+            ach = flops / tt / 1e12
+            return {"bound": "tensor", "achieved": round(ach, 1), "peak": round(fp8_peak, 1), "unit": "TFLOP/s",
+                    "frac": round(ach / fp8_peak, 3), "traffic": traffic, "kernel": name,
+                    "launch_shapes": [(r["m"], r["n"], r["k"]) for r in rows],
+                    "algorithmic_bytes_per_launch": byts / len(rows),
+                    "peak_source": f"{peak_src}: bf16 burst {peaks['bf16_tflops']} x {FP8_PER_BF16} "
+                                   "(nominal FP8/BF16 ratio)"}
+        ach = byts / tt / 1e9
+        return {"bound": "hbm", "achieved": round(ach, 1), "peak": hbm_peak, "unit": "GB/s",
+                "frac": round(ach / hbm_peak, 3), "traffic": traffic, "kernel": name,
+                "launch_shapes": [(r["m"], r["n"], r["k"]) for r in rows],
+                "algorithmic_bytes_per_launch": byts / len(rows), "peak_source": f"{peak_src}: hbm copy"}
 
-    ach_t = agg(tensor_bound, "flops")
-    ach_h = agg(hbm_bound, "bytes")
-    roofline = {"bound": "tensor", "achieved": round(ach_t, 1), "peak": round(fp8_peak, 1), "unit": "TFLOP/s",
-                "frac": round(ach_t / fp8_peak, 3), "traffic": None,
-                "kernel": "fg::fp8_gemm_kernel<256,4,dense> on the m=4096 shapes",
-                "peak_source": f"{peak_src}: bf16 burst {peaks['bf16_tflops']} x {FP8_PER_BF16} (nominal FP8/BF16)"}
-    roofline_hbm = {"bound": "hbm", "achieved": round(ach_h, 1), "peak": hbm_peak, "unit": "GB/s",
-                    "frac": round(ach_h / hbm_peak, 3), "traffic": None,
-                    "kernel": "fg::fp8_gemm_kernel<256,4,dense> on the m<=128 shapes",
-                    "peak_source": f"{peak_src}: hbm copy"}
+    by_time = sorted(kern_rows.items(), key=lambda kv: -sum(r["us"] for r in kv[1]))
+    roofline = roof(*by_time[0])
+    others = [roof(name, rows) for name, rows in by_time[1:]]
+    hbm_rows = [r for r in shape_rows if 2.0 * r["m"] * r["n"] * r["k"] / problem_bytes(r["m"], r["n"], r["k"]) < ridge]
+    roofline_hbm = None
+    if hbm_rows:
+        tt = sum(r["us"] for r in hbm_rows) * 1e-6
+        ach = sum(problem_bytes(r["m"], r["n"], r["k"]) for r in hbm_rows) / tt / 1e9
+        roofline_hbm = {"bound": "hbm", "achieved": round(ach, 1), "peak": hbm_peak, "unit": "GB/s",
+                        "frac": round(ach / hbm_peak, 3), "shapes": "all bandwidth-bound problems of the step",
+                        "peak_source": f"{peak_src}: hbm copy"}
 
     # ------------------------------------------------ end to end (host buffers)
     e2e = None
     if not args.no_e2e:
         host = []
-        for (m, n, k, A, sA, B, sB, D) in items:
+        for (m, n, k, copies) in items:
+            A, sA, B, sB, D = copies[0]
             p = probs[(n, k)]
             hA = torch.from_numpy(np.ascontiguousarray(p.A[:m])).pin_memory()
             hsA = torch.from_numpy(np.ascontiguousarray(p.sA[:m])).pin_memory()
@@ -383,12 +443,14 @@ def run_ours(args, ws, rank, local):
             "scaling": "weak", "vs_baseline": None, "dtype": "fp8_e4m3",
             "data": "synthetic (seeded N(0,1), quantized to E4M3 per 1x128 / 128x128 group)",
             "config": {"workload": WORKLOAD, "problems_per_step": len(items),
-                       "l2": "flushed before every launch (256 MiB write, outside the timed intervals)",
-                       "timing": "CUDA events around each launch on the launching stream, summed per step",
+                       "l2": ("inputs larger than L2: each problem rotates over identical copies of its "
+                              "inputs and output totalling >= 272 MiB (> 2 x L2)"),
+                       "timing": ("CUDA events on the launching stream around the K back-to-back launches "
+                                  "of each problem; per-problem times summed per step"),
                        "parallelism": f"replica x{ws} (independent problems per GPU)"},
             "hbm_gbs": round(ws * bytes_step / (step_ms * 1e-3) / 1e9, 1),
             "wall_ms_per_step": round(wall / args.steps * 1e3, 3),
-            "roofline": roofline, "roofline_hbm": roofline_hbm,
+            "roofline": roofline, "roofline_other_kernels": others, "roofline_hbm": roofline_hbm,
             "shapes": shape_rows, "clocks": clock_info, "e2e": e2e,
             "gpu_launches": len(items) * args.steps, "cpu_baseline": cpu,
         }

@@ -125,6 +125,11 @@ fg_status fg_set_num_sms(int num_sms);
  * by FP32 summation order. */
 fg_status fg_set_config_override(int block_n, int split_k);
 
+/* The tile plan a dense call of this shape would use on the current device:
+ * output tile width (*block_n) and split-K cluster size (*split_k, 1 = none).
+ * Host-only query (reads device attributes, launches nothing). */
+fg_status fg_query_dense_plan(int m, int n, int k, int *block_n, int *split_k);
+
 /* Watchdog limit of each in-kernel pipeline wait, in milliseconds (default
  * 2000; 0 restores the default). */
 fg_status fg_set_watchdog_ms(uint32_t ms);

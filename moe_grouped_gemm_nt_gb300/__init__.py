@@ -46,6 +46,7 @@ SIGNATURES = {
     "fg_set_num_sms": (_I, [_I]),
     "fg_set_watchdog_ms": (_I, [_U32]),
     "fg_set_config_override": (_I, [_I, _I]),
+    "fg_query_dense_plan": (_I, [_I, _I, _I, ctypes.POINTER(_I), ctypes.POINTER(_I)]),
     "fg_status_string": (ctypes.c_char_p, [_I]),
     "fg_version": (_I, []),
     "fg_debug_skip_producer_iteration": (_I, [_I]),
@@ -213,6 +214,13 @@ def fg_set_num_sms(n: int) -> None:
 def fg_set_config_override(block_n: int = 0, split_k: int = 0) -> None:
     """Force the dense tile plan (block_n 128/256, split_k 1..8; 0 = automatic)."""
     _check("fg_set_config_override", lib().fg_set_config_override(int(block_n), int(split_k)))
+
+
+def fg_query_dense_plan(m: int, n: int, k: int):
+    """(block_n, split_k) that a dense call of this shape would use."""
+    bn, sp = ctypes.c_int(0), ctypes.c_int(0)
+    _check("fg_query_dense_plan", lib().fg_query_dense_plan(int(m), int(n), int(k), ctypes.byref(bn), ctypes.byref(sp)))
+    return bn.value, sp.value
 
 
 def fg_set_watchdog_ms(ms: int) -> None:

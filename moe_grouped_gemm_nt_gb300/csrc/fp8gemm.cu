@@ -189,6 +189,42 @@ struct Plan {
     int split = 1;  // CTAs per output tile (one cluster); 1 = persistent walk
 };
 
+// ---- plan of a dense call: persistent 128 x 256 tiles when they fill the
+// GPU; otherwise (few output tiles, e.g. m <= 128) narrower tiles and/or
+// split-K clusters, so that about one wave of CTAs streams the operands.
+Plan choose_dense_plan(int m, int n, int k, int sms) {
+    Plan plan;
+    const int fbn = g_force_bn.load(), fsplit = g_force_split.load();
+    if (fbn != 0 || fsplit != 0) {
+        plan.bn = fbn == 128 ? 128 : 256;
+        plan.split = fsplit > 0 ? fsplit : 1;
+        return plan;
+    }
+    const int num_kb = cdiv(k, fg::BLOCK_K);
+    const long long m_blocks = cdiv(m, fg::BLOCK_M);
+    const long long tiles256 = m_blocks * cdiv(n, 256);
+    long long best = tiles256 < sms ? tiles256 : sms;
+    if (tiles256 * 4 >= (long long)sms * 3) return plan;
+    for (int bn : {256, 128}) {
+        const long long tiles = m_blocks * cdiv(n, bn);
+        for (int sp = 1; sp <= 8; ++sp) {
+            if (sp > 1 && num_kb < 2 * sp) break;  // at least two K blocks per rank
+            long long cap = sms;
+            if (sp > 1)
+                cap = (long long)sp * (bn == 256 ? Kernel<256, 4, fg::KIND_DENSE, true>::max_active_clusters(sp)
+                                                 : Kernel<128, 6, fg::KIND_DENSE, true>::max_active_clusters(sp));
+            const long long ctas = tiles * sp;
+            if (ctas > cap) continue;  // more than one wave
+            if (ctas > best) {
+                best = ctas;
+                plan.bn = bn;
+                plan.split = sp;
+            }
+        }
+    }
+    return plan;
+}
+
 bool fmt_ok(int f) { return f == FG_E4M3 || f == FG_E5M2; }
 
 // M blocks per raster group: as many as keep the group's A rows (128 x k bytes
@@ -227,45 +263,12 @@ fg_status run(const void *A, int a_fmt, const float *sA, int ld_sA, const void *
     DeviceInfo *dev = nullptr;
     if (fg_status st = device_info(&dev); st != FG_OK) return st;
 
-    // ---- plan: persistent 128 x 256 tiles when they fill the GPU; otherwise
-    // (few output tiles, e.g. m <= 128) narrower tiles and/or split-K clusters
-    // so that about one wave of CTAs streams the operands.
     int sms = dev->num_sms;
     const int ovr = g_num_sms_override.load();
     if (ovr > 0 && ovr < sms) sms = ovr;
     const int num_kb = cdiv(k, fg::BLOCK_K);
     const long long m_blocks_total = (long long)cdiv(rows, fg::BLOCK_M) * (KIND == fg::KIND_MASKED ? G : 1);
-    Plan plan;
-    if (KIND == fg::KIND_DENSE) {
-        const int fbn = g_force_bn.load(), fsplit = g_force_split.load();
-        if (fbn != 0 || fsplit != 0) {
-            plan.bn = fbn == 128 ? 128 : 256;
-            plan.split = fsplit > 0 ? fsplit : 1;
-        } else {
-            const long long tiles256 = m_blocks_total * cdiv(n, 256);
-            long long best = tiles256 < sms ? tiles256 : sms;
-            if (tiles256 * 4 < (long long)sms * 3) {
-                for (int bn : {256, 128}) {
-                    const long long tiles = m_blocks_total * cdiv(n, bn);
-                    for (int sp = 1; sp <= 8; ++sp) {
-                        if (sp > 1 && num_kb < 2 * sp) break;  // at least two K blocks per rank
-                        long long cap = sms;
-                        if (sp > 1)
-                            cap = (long long)sp * (bn == 256
-                                                       ? Kernel<256, 4, fg::KIND_DENSE, true>::max_active_clusters(sp)
-                                                       : Kernel<128, 6, fg::KIND_DENSE, true>::max_active_clusters(sp));
-                        const long long ctas = tiles * sp;
-                        if (ctas > cap) continue;  // more than one wave
-                        if (ctas > best) {
-                            best = ctas;
-                            plan.bn = bn;
-                            plan.split = sp;
-                        }
-                    }
-                }
-            }
-        }
-    }
+    const Plan plan = KIND == fg::KIND_DENSE ? choose_dense_plan(rows, n, k, sms) : Plan{};
     const int BN = plan.bn;
 
     CUtensorMap ta, tb, td, tsa;
@@ -367,6 +370,19 @@ fg_status fg_get_device_status(void *stream, uint32_t *detail) {
 fg_status fg_set_num_sms(int num_sms) {
     if (num_sms < 0) return FG_ERR_INVALID_ARG;
     g_num_sms_override.store(num_sms);
+    return FG_OK;
+}
+
+fg_status fg_query_dense_plan(int m, int n, int k, int *block_n, int *split_k) {
+    if (m < 1 || n < 1 || k < 1 || !block_n || !split_k) return FG_ERR_INVALID_ARG;
+    DeviceInfo *dev = nullptr;
+    if (fg_status st = device_info(&dev); st != FG_OK) return st;
+    int sms = dev->num_sms;
+    const int ovr = g_num_sms_override.load();
+    if (ovr > 0 && ovr < sms) sms = ovr;
+    const Plan plan = choose_dense_plan(m, n, k, sms);
+    *block_n = plan.bn;
+    *split_k = plan.split;
     return FG_OK;
 }
 

@@ -25,7 +25,7 @@
  *
  * Pins: every function here is checked by tests/test_oracle_pins.py against
  * values fixed by the pages (format widths and maxima of E4M3/E5M2, page
- * "DeepGEMM: FP8 GEMM on Hopper" section 3.1 table), closed forms, brute force
+ * "DeepGEMM：基于 Hopper Tensor Core 的 FP8 矩阵乘法内核优化实践" section 3.1 table), closed forms, brute force
  * over all FP8 codes, library routines on special cases (numpy float64 matmul
  * with unit scales, torch's float8 and bfloat16 conversions) and invariants
  * (zero scales, power-of-two scale linearity, grouped == per-group dense).

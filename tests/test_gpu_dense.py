@@ -46,7 +46,7 @@ def test_boundary_shapes(m, n, k):
 
 def test_p1_regression_shape_6144_1280():
     """The tutorial's intermittent failure shape M = N = 6144, K = 1280 (page
-    "DeepGEMM: FP8 GEMM on Hopper", section 6), checked on sampled outputs,
+    "DeepGEMM：基于 Hopper Tensor Core 的 FP8 矩阵乘法内核优化实践", section 6), checked on sampled outputs,
     three times in a row."""
     p = wl.dense(6144, 6144, 1280, seed=4242)
     rows, cols = sample_positions(p.m, p.n, seed=1, n_rows_full=4)

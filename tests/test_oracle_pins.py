@@ -1,7 +1,7 @@
 """Pins of the CPU oracle against facts that do not come from the oracle itself.
 
 Each test ties one part of the oracle to something fixed outside it: the FP8
-format table of the page "DeepGEMM: FP8 GEMM on Hopper" (section 3.1), hand
+format table of the page "DeepGEMM：基于 Hopper Tensor Core 的 FP8 矩阵乘法内核优化实践" (section 3.1), hand
 decoded bytes, torch's float8/bfloat16 conversions, numpy's float64 matmul on
 the unit-scale special case, closed forms, brute force over all FP8 codes and
 invariants of the definition (zero scales, power-of-two linearity, grouped

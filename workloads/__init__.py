@@ -5,7 +5,7 @@ no arithmetic of the GEMM itself: it draws seeded N(0,1) values, quantizes them
 to FP8 the way the input recipe asks (one FP32 scale ``amax / fp8_max`` per
 1x128 row group of the LHS and per 128x128 block of the RHS, as in the page
 "DeepSeek开源周第三天DeepGEMM", section "基本用法", with maxima 448 for E4M3 and
-57344 for E5M2 from "DeepGEMM: FP8 GEMM on Hopper", section 3.1), builds the
+57344 for E5M2 from "DeepGEMM：基于 Hopper Tensor Core 的 FP8 矩阵乘法内核优化实践", section 3.1), builds the
 grouped index tensors, and rearranges scale tensors between layouts.
 
 FP8 encoding uses torch's float8 conversions (round to nearest even) after
