@@ -117,7 +117,7 @@ fg_status fg_get_device_status(void *stream, uint32_t *detail);
  * ("SM资源控制"); 0 restores the default (all SMs). */
 fg_status fg_set_num_sms(int num_sms);
 
-/* Tuning / testing override of the tile plan of later dense calls: block_n
+/* Tuning / testing override of the tile plan of later calls: block_n
  * (output tile width, 128 or 256; 0 = automatic) and split_k (number of CTAs,
  * one thread-block cluster, that share the K blocks of one output tile and
  * reduce their partials through distributed shared memory in a fixed order;

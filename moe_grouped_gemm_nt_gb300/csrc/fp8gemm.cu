@@ -189,10 +189,12 @@ struct Plan {
     int split = 1;  // CTAs per output tile (one cluster); 1 = persistent walk
 };
 
-// ---- plan of a dense call: persistent 128 x 256 tiles when they fill the
-// GPU; otherwise (few output tiles, e.g. m <= 128) narrower tiles and/or
-// split-K clusters, so that about one wave of CTAs streams the operands.
-Plan choose_dense_plan(int m, int n, int k, int sms) {
+// ---- plan of a call with `m_blocks` 128-row blocks (grouped layouts: all
+// groups; masked: the capacity, as the counts live on the device): persistent
+// 128 x 256 tiles when they fill the GPU; otherwise (few output tiles, e.g.
+// m <= 128) narrower tiles and/or split-K clusters, so that about one wave of
+// CTAs streams the operands.
+Plan choose_plan(long long m_blocks, int n, int k, int sms) {
     Plan plan;
     const int fbn = g_force_bn.load(), fsplit = g_force_split.load();
     if (fbn != 0 || fsplit != 0) {
@@ -201,7 +203,6 @@ Plan choose_dense_plan(int m, int n, int k, int sms) {
         return plan;
     }
     const int num_kb = cdiv(k, fg::BLOCK_K);
-    const long long m_blocks = cdiv(m, fg::BLOCK_M);
     const long long tiles256 = m_blocks * cdiv(n, 256);
     long long best = tiles256 < sms ? tiles256 : sms;
     if (tiles256 * 4 >= (long long)sms * 3) return plan;
@@ -268,7 +269,7 @@ fg_status run(const void *A, int a_fmt, const float *sA, int ld_sA, const void *
     if (ovr > 0 && ovr < sms) sms = ovr;
     const int num_kb = cdiv(k, fg::BLOCK_K);
     const long long m_blocks_total = (long long)cdiv(rows, fg::BLOCK_M) * (KIND == fg::KIND_MASKED ? G : 1);
-    const Plan plan = KIND == fg::KIND_DENSE ? choose_dense_plan(rows, n, k, sms) : Plan{};
+    const Plan plan = choose_plan(m_blocks_total, n, k, sms);
     const int BN = plan.bn;
 
     CUtensorMap ta, tb, td, tsa;
@@ -301,7 +302,7 @@ fg_status run(const void *A, int a_fmt, const float *sA, int ld_sA, const void *
     p.debug_skip_iter = g_debug_skip_iter.exchange(-1);
 
     const long long max_tiles = m_blocks_total * p.num_n_blocks;
-    if constexpr (KIND == fg::KIND_DENSE) {
+    {
         if (plan.split > 1) {
             // one cluster of `split` CTAs per output tile
             const long long grid = max_tiles * plan.split;
@@ -380,7 +381,7 @@ fg_status fg_query_dense_plan(int m, int n, int k, int *block_n, int *split_k) {
     int sms = dev->num_sms;
     const int ovr = g_num_sms_override.load();
     if (ovr > 0 && ovr < sms) sms = ovr;
-    const Plan plan = choose_dense_plan(m, n, k, sms);
+    const Plan plan = choose_plan(cdiv(m, fg::BLOCK_M), n, k, sms);
     *block_n = plan.bn;
     *split_k = plan.split;
     return FG_OK;

@@ -198,3 +198,28 @@ def test_masked_workload(G, n, k):
     C_ = np.concatenate([cols, extra_c]).astype(np.int64)
     ref, _ = oracle.grouped_masked_at(p.A, 0, p.sA, p.B, 0, p.sB, p.masked_m, G_, R_, C_)
     compare(got[G_, R_, C_], ref, what=f"masked G={G} n={n} k={k} (sampled)")
+
+
+@pytest.mark.parametrize("bn,split", [(256, 2), (128, 3), (256, 5), (128, 8)])
+def test_grouped_split_plans_match_oracle(bn, split):
+    """Split-K clusters on the grouped layouts: tiles past the device-side
+    counts, padding tiles and untouched rows behave as in the persistent walk."""
+    fg.fg_set_config_override(bn, split)
+    try:
+        p = wl.masked(6, 256, n=264, k=1040, seed=61, masked_m=[0, 1, 127, 128, 129, 256])
+        got = d_to_bits(run_masked(p))
+        init = np.full((p.G, p.M_cap, p.n), SENTINEL, np.uint16)
+        ref, _ = oracle.grouped_masked(p.A, 0, p.sA, p.B, 0, p.sB, p.masked_m, init)
+        valid = np.arange(p.M_cap)[None, :] < p.masked_m[:, None]
+        assert np.array_equal(got[~valid], ref[~valid])
+        compare(got[valid], ref[valid], what=f"masked split bn={bn} s={split}")
+
+        c = wl.contiguous([100, 0, 300, 5, 128], n=264, k=1040, seed=62)
+        got = d_to_bits(run_contiguous(c))
+        init = np.full((c.M, c.n), SENTINEL, np.uint16)
+        ref, _ = oracle.grouped_contiguous(c.A, 0, c.sA, c.B, 0, c.sB, c.m_indices, init)
+        pad = c.m_indices < 0
+        assert np.array_equal(got[pad], ref[pad])
+        compare(got[~pad], ref[~pad], what=f"contiguous split bn={bn} s={split}")
+    finally:
+        fg.fg_set_config_override(0, 0)
