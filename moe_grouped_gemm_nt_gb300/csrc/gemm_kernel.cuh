@@ -70,7 +70,8 @@ constexpr int STAGING_BYTES_PER_WARP = 32 * 128;  // 32 rows x 64 BF16 columns
 constexpr int A_STAGE_BYTES = BLOCK_M * BLOCK_K;
 constexpr int SA_STAGE_BYTES = BLOCK_M * 4;      // 128 LHS scales of one K block
 constexpr int SB_STAGE_BYTES = 16;               // the RHS scales of the two column halves
-constexpr int SCALE_STAGES = 4;
+constexpr int SCALE_STAGES = 4;  // a power of two
+static_assert((SCALE_STAGES & (SCALE_STAGES - 1)) == 0, "scale ring size");
 
 struct GemmParams {
     int rows;          // rows of the A / D row space: dense m, contiguous M, masked M_cap
@@ -187,11 +188,22 @@ __device__ __forceinline__ Tile get_tile(const GemmParams &p, int t, int mblocks
     return ti;
 }
 
+__device__ __noinline__ bool wait_phase_slow(uint32_t bar, uint32_t parity, volatile uint32_t *abort_flag,
+                                             const GemmParams &p, uint32_t role);
+
 // Bounded wait on an mbarrier phase.  Returns false on watchdog expiry (after
 // recording it and raising the CTA abort flag) or when another role aborted.
+// The first probe is inline; the spin loop with its timer and abort checks is
+// kept out of line so the hot loops stay small (the promotion warps are
+// issue-bound).
 __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile uint32_t *abort_flag,
                                            const GemmParams &p, uint32_t role) {
     if (mbar_try_wait(bar, parity)) return true;
+    return wait_phase_slow(bar, parity, abort_flag, p, role);
+}
+
+__device__ __noinline__ bool wait_phase_slow(uint32_t bar, uint32_t parity, volatile uint32_t *abort_flag,
+                                             const GemmParams &p, uint32_t role) {
     const uint64_t t0 = global_timer_ns();
     uint32_t spins = 0;
     while (!mbar_try_wait(bar, parity)) {
@@ -427,7 +439,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const uint32_t t_lane = (uint32_t)(sub * 32) << 16;
         const uint32_t sa_addr = sbase + L::SA_OFF + r * 4;
         const uint32_t sb_addr = sbase + L::SB_OFF + half * 4;
-        uint32_t it = 0;
+        const uint32_t t_base = tmem_base + t_lane + half * COLS;
+        // ring positions, advanced incrementally: TMEM buffer b (phase bph) and
+        // scale-ring entry q (phase qph) of the current K iteration
+        uint32_t b = 0, bph = 0, q = 0, qph = 0;
         bool ok = true;
         for (int t = t_begin; t < num_tiles && ok; t += t_step) {
             const Tile ti = get_tile<BN, KIND>(p, t, m_blocks);
@@ -448,9 +463,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
             for (int j = 0; j < COLS / 2; ++j) acc2[j] = 0ull;
 
-            for (int kb = kb_begin; kb < kb_end; ++kb, ++it) {
-                const uint32_t b = it & 1u, bph = (it >> 1) & 1u;
-                const uint32_t q = it % SCALE_STAGES, qph = (it / SCALE_STAGES) & 1u;
+            for (int kb = kb_begin; kb < kb_end; ++kb) {
                 const bool got = wait_phase(sfull_bar(q), qph, abort_flag, p, ROLE_EPILOGUE) &&
                                  wait_phase(tfull_bar(b), bph, abort_flag, p, ROLE_EPILOGUE);
                 if (!__all_sync(0xffffffffu, got)) {
@@ -463,7 +476,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(sempty_bar(q));
                 const uint64_t sc2 = pack_f32x2(sc, sc);
-                const uint32_t taddr = tmem_base + t_lane + b * BN + half * COLS;
+                const uint32_t taddr = t_base + b * BN;
 #pragma unroll
                 for (int c = 0; c < COLS / TMEM_LD_COLS; ++c) {
                     uint32_t v[TMEM_LD_COLS];
@@ -483,6 +496,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     for (int j = 0; j < TMEM_LD_COLS; j += 2)
                         ffma2(acc2[(c * TMEM_LD_COLS + j) / 2], v[j], v[j + 1], sc2);
                 }
+                b ^= 1u;
+                bph ^= (b == 0u);
+                q = (q + 1u) & (SCALE_STAGES - 1u);
+                qph ^= (q == 0u);
             }
             if (!ok) break;
 
