@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cstdint>
 #include <cstdlib>
@@ -190,11 +191,40 @@ struct Plan {
 };
 
 // ---- plan of a call with `m_blocks` 128-row blocks (grouped layouts: all
-// groups; masked: the capacity, as the counts live on the device): persistent
-// 128 x 256 tiles when they fill the GPU; otherwise (few output tiles, e.g.
-// m <= 128) narrower tiles and/or split-K clusters, so that about one wave of
-// CTAs streams the operands.
-Plan choose_plan(long long m_blocks, int n, int k, int sms) {
+// groups; masked: the capacity, as the counts live on the device) and at most
+// `rows` valid rows per 128-row block.  Persistent 128 x 256 tiles when they
+// fill the GPU.  Otherwise (few output tiles, e.g. m <= 128) the tile width
+// and split-K cluster size with the lowest estimated time:
+//   start-up + max(HBM time, K blocks per CTA x K-block time) x waves
+//   + (split-K) cluster barrier + partial exchange through distributed smem.
+// The constants were measured on GB300 (per-phase timestamps in the kernel,
+// a distributed-shared-memory microbenchmark) and rank the measured plans of
+// the small-m problems correctly.
+constexpr double kStartUs = 3.5;         // launch to first operand bytes
+constexpr double kKBlockUs256 = 0.50;    // one 128 x 256 x 128 K block, promotion included
+constexpr double kKBlockUs128 = 0.35;    // one 128 x 128 x 128 K block
+constexpr double kHbmBytesPerUs = 6.5e6; // sustained HBM bandwidth
+constexpr double kDsmemBytesPerUs = 3.4e4;  // per-SM distributed shared memory bandwidth
+constexpr double kReduceSyncUs = 1.0;    // the cluster barriers around the exchange
+
+double plan_cost(long long m_blocks, int rows, int n, int k, int bn, int split, long long cap_ctas) {
+    const long long kb = cdiv(k, fg::BLOCK_K);
+    const long long tiles = m_blocks * cdiv(n, bn);
+    const long long ctas = tiles * split;
+    const long long waves = (ctas + cap_ctas - 1) / cap_ctas;
+    const double kb_per_cta = (double)((kb + split - 1) / split) * (double)waves;
+    const double rows_total = (double)(rows < m_blocks * fg::BLOCK_M ? rows : m_blocks * fg::BLOCK_M);
+    const double hbm_us = (rows_total * k + (double)n * k + rows_total * n * 2.0) / kHbmBytesPerUs;
+    const double main_us = std::max(hbm_us, kb_per_cta * (bn == 256 ? kKBlockUs256 : kKBlockUs128));
+    double red_us = 0.0;
+    if (split > 1) {
+        const double tile_rows = rows < fg::BLOCK_M ? rows : fg::BLOCK_M;
+        red_us = kReduceSyncUs + tile_rows * bn * 4.0 * (split - 1) / split / kDsmemBytesPerUs;
+    }
+    return kStartUs + main_us + red_us;
+}
+
+Plan choose_plan(long long m_blocks, int rows, int n, int k, int sms) {
     Plan plan;
     const int fbn = g_force_bn.load(), fsplit = g_force_split.load();
     if (fbn != 0 || fsplit != 0) {
@@ -204,20 +234,22 @@ Plan choose_plan(long long m_blocks, int n, int k, int sms) {
     }
     const int num_kb = cdiv(k, fg::BLOCK_K);
     const long long tiles256 = m_blocks * cdiv(n, 256);
-    long long best = tiles256 < sms ? tiles256 : sms;
     if (tiles256 * 4 >= (long long)sms * 3) return plan;
+    double best = 1e30;
     for (int bn : {256, 128}) {
-        const long long tiles = m_blocks * cdiv(n, bn);
         for (int sp = 1; sp <= 8; ++sp) {
             if (sp > 1 && num_kb < 2 * sp) break;  // at least two K blocks per rank
             long long cap = sms;
-            if (sp > 1)
-                cap = (long long)sp * (bn == 256 ? Kernel<256, 4, fg::KIND_DENSE, true>::max_active_clusters(sp)
-                                                 : Kernel<128, 6, fg::KIND_DENSE, true>::max_active_clusters(sp));
-            const long long ctas = tiles * sp;
-            if (ctas > cap) continue;  // more than one wave
-            if (ctas > best) {
-                best = ctas;
+            if (sp > 1) {
+                const int clusters = bn == 256 ? Kernel<256, 4, fg::KIND_DENSE, true>::max_active_clusters(sp)
+                                               : Kernel<128, 6, fg::KIND_DENSE, true>::max_active_clusters(sp);
+                cap = (long long)sp * clusters;
+                // a second wave of clusters would pay start-up and exchange again
+                if (cap <= 0 || m_blocks * cdiv(n, bn) * sp > cap) continue;
+            }
+            const double c = plan_cost(m_blocks, rows, n, k, bn, sp, cap);
+            if (c < best) {
+                best = c;
                 plan.bn = bn;
                 plan.split = sp;
             }
@@ -269,7 +301,7 @@ fg_status run(const void *A, int a_fmt, const float *sA, int ld_sA, const void *
     if (ovr > 0 && ovr < sms) sms = ovr;
     const int num_kb = cdiv(k, fg::BLOCK_K);
     const long long m_blocks_total = (long long)cdiv(rows, fg::BLOCK_M) * (KIND == fg::KIND_MASKED ? G : 1);
-    const Plan plan = choose_plan(m_blocks_total, n, k, sms);
+    const Plan plan = choose_plan(m_blocks_total, KIND == fg::KIND_DENSE ? rows : INT32_MAX, n, k, sms);
     const int BN = plan.bn;
 
     CUtensorMap ta, tb, td, tsa;
@@ -381,7 +413,7 @@ fg_status fg_query_dense_plan(int m, int n, int k, int *block_n, int *split_k) {
     int sms = dev->num_sms;
     const int ovr = g_num_sms_override.load();
     if (ovr > 0 && ovr < sms) sms = ovr;
-    const Plan plan = choose_plan(cdiv(m, fg::BLOCK_M), n, k, sms);
+    const Plan plan = choose_plan(cdiv(m, fg::BLOCK_M), m, n, k, sms);
     *block_n = plan.bn;
     *split_k = plan.split;
     return FG_OK;

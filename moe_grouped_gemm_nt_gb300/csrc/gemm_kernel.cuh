@@ -286,45 +286,51 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
 
     // ------------------------------------------------------------- set-up
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) {
-            mbar_init(full_bar(s), 1);
-            mbar_init(empty_bar(s), 1);
+    // The producer warp initializes the barriers and starts loading right
+    // away; the other warps wait (named barrier 1) for the barriers and for the
+    // TMEM allocation, which only they need.
+    if (warp == PRODUCER_WARP) {
+        if (lane == 0) {
+            prefetch_tensormap(&tmap_a);
+            prefetch_tensormap(&tmap_b);
+            prefetch_tensormap(&tmap_sa);
+            prefetch_tensormap(&tmap_d);
+            for (int s = 0; s < STAGES; ++s) {
+                mbar_init(full_bar(s), 1);
+                mbar_init(empty_bar(s), 1);
+            }
+            for (int q = 0; q < SCALE_STAGES; ++q) {
+                mbar_init(sfull_bar(q), 2);  // producer's expect_tx arrival + the cp.async arrival
+                mbar_init(sempty_bar(q), NUM_EPI_WARPS);
+            }
+            for (int b = 0; b < 2; ++b) {
+                mbar_init(tfull_bar(b), 1);
+                mbar_init(tempty_bar(b), NUM_EPI_WARPS);
+            }
+            mbar_init(drain_bar, 1);
+            *abort_flag = 0u;
+            fence_mbarrier_init();
         }
-        for (int q = 0; q < SCALE_STAGES; ++q) {
-            mbar_init(sfull_bar(q), 2);  // producer's expect_tx arrival + the cp.async arrival
-            mbar_init(sempty_bar(q), NUM_EPI_WARPS);
+        __syncwarp();
+        named_bar_arrive(1, NUM_THREADS);
+    } else {
+        if (warp == MMA_WARP) {
+            tmem_alloc(smem_u32(tmem_slot), L::TMEM_COLS);
+            tmem_relinquish();
         }
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(tfull_bar(b), 1);
-            mbar_init(tempty_bar(b), NUM_EPI_WARPS);
-        }
-        mbar_init(drain_bar, 1);
-        *abort_flag = 0u;
-        fence_mbarrier_init();
-    }
-    if (warp == MMA_WARP) {
-        tmem_alloc(smem_u32(tmem_slot), L::TMEM_COLS);
-        tmem_relinquish();
-    }
-    if (warp == PRODUCER_WARP && lane == 0) {
-        prefetch_tensormap(&tmap_a);
-        prefetch_tensormap(&tmap_b);
-        prefetch_tensormap(&tmap_d);
-        prefetch_tensormap(&tmap_sa);
-    }
-    if constexpr (KIND == KIND_MASKED) {
-        if (blockIdx.x == 0 && warp == 0) {
-            for (int g = lane; g < p.num_groups; g += 32) {
-                const int c = __ldg(p.masked_m + g);
-                if (c < 0 || c > p.rows) record_error(p, DEV_ERR_CHECK, (uint32_t)g);
+        if constexpr (KIND == KIND_MASKED) {
+            if (blockIdx.x == 0 && warp == 0) {
+                for (int g = lane; g < p.num_groups; g += 32) {
+                    const int c = __ldg(p.masked_m + g);
+                    if (c < 0 || c > p.rows) record_error(p, DEV_ERR_CHECK, (uint32_t)g);
+                }
             }
         }
+        tc_fence_before();
+        named_bar_sync(1, NUM_THREADS);
+        tc_fence_after();
     }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem_base = *tmem_slot;
+    const uint32_t tmem_base = warp == PRODUCER_WARP ? 0u : *tmem_slot;  // the producer never uses TMEM
 
     const int m_blocks = total_m_blocks<KIND>(p);
     const int num_tiles = m_blocks * p.num_n_blocks;
