@@ -130,6 +130,13 @@ fg_status fg_set_config_override(int block_n, int split_k);
  * Host-only query (reads device attributes, launches nothing). */
 fg_status fg_query_dense_plan(int m, int n, int k, int *block_n, int *split_k);
 
+/* Programmatic dependent launch of the GEMM kernels (default on): a call's
+ * CTAs may start while the previous kernel of the stream finishes, set up
+ * their shared memory, tensor memory and barriers, and wait for the previous
+ * kernel to complete before their first global-memory access.  The results
+ * are the same either way; 0 turns it off for later calls. */
+fg_status fg_set_programmatic_launch(int enable);
+
 /* Watchdog limit of each in-kernel pipeline wait, in milliseconds (default
  * 2000; 0 restores the default). */
 fg_status fg_set_watchdog_ms(uint32_t ms);

@@ -46,6 +46,7 @@ SIGNATURES = {
     "fg_set_num_sms": (_I, [_I]),
     "fg_set_watchdog_ms": (_I, [_U32]),
     "fg_set_config_override": (_I, [_I, _I]),
+    "fg_set_programmatic_launch": (_I, [_I]),
     "fg_query_dense_plan": (_I, [_I, _I, _I, ctypes.POINTER(_I), ctypes.POINTER(_I)]),
     "fg_status_string": (ctypes.c_char_p, [_I]),
     "fg_version": (_I, []),
@@ -221,6 +222,10 @@ def fg_query_dense_plan(m: int, n: int, k: int):
     bn, sp = ctypes.c_int(0), ctypes.c_int(0)
     _check("fg_query_dense_plan", lib().fg_query_dense_plan(int(m), int(n), int(k), ctypes.byref(bn), ctypes.byref(sp)))
     return bn.value, sp.value
+
+
+def fg_set_programmatic_launch(enable: bool) -> None:
+    _check("fg_set_programmatic_launch", lib().fg_set_programmatic_launch(1 if enable else 0))
 
 
 def fg_set_watchdog_ms(ms: int) -> None:

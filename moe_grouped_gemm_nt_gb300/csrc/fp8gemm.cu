@@ -111,24 +111,37 @@ bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0
 int cdiv(int a, int b) { return (a + b - 1) / b; }
 
 std::atomic<int> g_force_bn{0};
+std::atomic<int> g_pdl{1};  // programmatic dependent launch of the GEMM kernels
 std::atomic<int> g_force_split{0};
 
 template <int BN, int STAGES, int KIND, bool SPLITK>
 struct Kernel {
     using L = fg::SmemLayout<BN, STAGES>;
 
-    static cudaLaunchConfig_t config(int grid, int cluster, cudaStream_t stream, cudaLaunchAttribute *at) {
+    // launch configuration: a cluster dimension (split-K) and/or programmatic
+    // dependent launch (`at` holds room for two attributes)
+    static cudaLaunchConfig_t config(int grid, int cluster, cudaStream_t stream, cudaLaunchAttribute *at,
+                                     bool pdl = false) {
         cudaLaunchConfig_t cfg{};
         cfg.gridDim = dim3(grid, 1, 1);
         cfg.blockDim = dim3(fg::NUM_THREADS, 1, 1);
         cfg.dynamicSmemBytes = L::BYTES;
         cfg.stream = stream;
-        at[0].id = cudaLaunchAttributeClusterDimension;
-        at[0].val.clusterDim.x = cluster;
-        at[0].val.clusterDim.y = 1;
-        at[0].val.clusterDim.z = 1;
+        unsigned n = 0;
+        if (cluster > 1 || SPLITK) {
+            at[n].id = cudaLaunchAttributeClusterDimension;
+            at[n].val.clusterDim.x = cluster;
+            at[n].val.clusterDim.y = 1;
+            at[n].val.clusterDim.z = 1;
+            ++n;
+        }
+        if (pdl) {
+            at[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+            at[n].val.programmaticStreamSerializationAllowed = 1;
+            ++n;
+        }
         cfg.attrs = at;
-        cfg.numAttrs = 1;
+        cfg.numAttrs = n;
         return cfg;
     }
 
@@ -154,7 +167,7 @@ struct Kernel {
         const int v = cache[dev][cluster].load();
         if (v > 0) return v;
         if (!configure()) return 0;
-        cudaLaunchAttribute at[1];
+        cudaLaunchAttribute at[2];
         cudaLaunchConfig_t cfg = config(cluster, cluster, nullptr, at);
         int n = 0;
         if (cudaOccupancyMaxActiveClusters(&n, fg::fp8_gemm_kernel<BN, STAGES, KIND, SPLITK>, &cfg) !=
@@ -170,16 +183,10 @@ struct Kernel {
                             const CUtensorMap &tsa, const GemmParams &p, int grid, int cluster,
                             cudaStream_t stream) {
         if (!configure()) return cuda_fail();
-        if constexpr (!SPLITK) {
-            fg::fp8_gemm_kernel<BN, STAGES, KIND, SPLITK><<<grid, fg::NUM_THREADS, L::BYTES, stream>>>(
-                ta, tb, td, tsa, p);
-        } else {
-            cudaLaunchAttribute at[1];
-            cudaLaunchConfig_t cfg = config(grid, cluster, stream, at);
-            if (cudaLaunchKernelEx(&cfg, fg::fp8_gemm_kernel<BN, STAGES, KIND, SPLITK>, ta, tb, td, tsa, p) !=
-                cudaSuccess)
-                return cuda_fail();
-        }
+        cudaLaunchAttribute at[2];
+        cudaLaunchConfig_t cfg = config(grid, cluster, stream, at, g_pdl.load() != 0);
+        if (cudaLaunchKernelEx(&cfg, fg::fp8_gemm_kernel<BN, STAGES, KIND, SPLITK>, ta, tb, td, tsa, p) != cudaSuccess)
+            return cuda_fail();
         return cudaPeekAtLastError() == cudaSuccess ? FG_OK : cuda_fail();
     }
 };
@@ -416,6 +423,11 @@ fg_status fg_query_dense_plan(int m, int n, int k, int *block_n, int *split_k) {
     const Plan plan = choose_plan(cdiv(m, fg::BLOCK_M), m, n, k, sms);
     *block_n = plan.bn;
     *split_k = plan.split;
+    return FG_OK;
+}
+
+fg_status fg_set_programmatic_launch(int enable) {
+    g_pdl.store(enable ? 1 : 0);
     return FG_OK;
 }
 

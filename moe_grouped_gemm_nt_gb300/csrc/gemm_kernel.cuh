@@ -40,6 +40,11 @@
 // slice of rows over all S partials through distributed shared memory, in rank
 // order (deterministic), and stores it as BF16.  No global scratch memory.
 //
+// Launch: programmatic dependent launch is enabled, so a grid may start while
+// the previous grid of the stream drains; each CTA sets up its barriers, TMEM
+// and tensor-map prefetches first and waits (griddepcontrol.wait) before its
+// first access to global memory.
+//
 // Every wait is bounded by a %globaltimer watchdog: on expiry the kernel
 // records FG_ERR_TIMEOUT in the status word, raises a CTA-wide abort flag,
 // waits (bounded) for its own copies and MMAs in flight, frees TMEM and exits.
@@ -318,19 +323,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             tmem_alloc(smem_u32(tmem_slot), L::TMEM_COLS);
             tmem_relinquish();
         }
-        if constexpr (KIND == KIND_MASKED) {
-            if (blockIdx.x == 0 && warp == 0) {
-                for (int g = lane; g < p.num_groups; g += 32) {
-                    const int c = __ldg(p.masked_m + g);
-                    if (c < 0 || c > p.rows) record_error(p, DEV_ERR_CHECK, (uint32_t)g);
-                }
-            }
-        }
         tc_fence_before();
         named_bar_sync(1, NUM_THREADS);
         tc_fence_after();
     }
     const uint32_t tmem_base = warp == PRODUCER_WARP ? 0u : *tmem_slot;  // the producer never uses TMEM
+
+    // Everything above touches only this CTA's own resources; global memory
+    // may still be in use by the previous grid of the stream until here.
+    griddep_wait();
+    griddep_launch_dependents();
+    if constexpr (KIND == KIND_MASKED) {
+        if (blockIdx.x == 0 && warp == 0) {
+            for (int g = lane; g < p.num_groups; g += 32) {
+                const int c = __ldg(p.masked_m + g);
+                if (c < 0 || c > p.rows) record_error(p, DEV_ERR_CHECK, (uint32_t)g);
+            }
+        }
+    }
 
     const int m_blocks = total_m_blocks<KIND>(p);
     const int num_tiles = m_blocks * p.num_n_blocks;

@@ -61,6 +61,15 @@ __device__ __forceinline__ void named_bar_arrive(uint32_t id, uint32_t count) {
     asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
+// Programmatic dependent launch: wait until the grids this one depends on
+// have completed and their memory is visible; allow the next grid in the
+// stream to start launching (its CTAs then wait in their own griddep_wait()).
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ----------------------------------------------------------------------- TMA
 
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map) {

@@ -167,3 +167,40 @@ def test_split_plans_agree_and_repeat(plan_override):
     ref16, _ = oracle.gemm_fp8_nt(p.A, 0, p.sA, p.B, 0, p.sB, want_f64=False)
     compare(a, ref16, what="split 4")
     compare(b, ref16, what="persistent")
+
+
+def test_programmatic_launch_keeps_stream_order():
+    """Back-to-back calls on one stream, with programmatic dependent launch on:
+    a call that overwrites the previous call's output (write after write), and a
+    call whose inputs were just written by the previous kernel (read after
+    write), give the same bits as with the launches fully serialized."""
+    import moe_grouped_gemm_nt_gb300 as fg
+    from gpu_common import dev, fp8_dtype
+
+    p1 = wl.dense(128, 4096, 7168, seed=81)   # split-K plan
+    p2 = wl.dense(128, 4096, 7168, seed=82)
+    p3 = wl.dense(1024, 2048, 2048, seed=83)  # persistent plan
+    def args(p):
+        return (dev(p.A, fp8_dtype(0)), fg.fg_scales_a_to_mn_major(dev(p.sA)), dev(p.B, fp8_dtype(0)), dev(p.sB))
+    a1, a2, a3 = args(p1), args(p2), args(p3)
+    results = {}
+    for pdl in (False, True):
+        fg.fg_set_programmatic_launch(pdl)
+        try:
+            D = torch.empty((128, 4096), dtype=torch.bfloat16, device="cuda")
+            A3 = torch.empty_like(a3[0])
+            D3 = torch.empty((1024, 2048), dtype=torch.bfloat16, device="cuda")
+            for _ in range(3):
+                fg.fg_gemm_fp8_nt(*a1, D)
+                fg.fg_gemm_fp8_nt(*a2, D)          # must land after the first
+                A3.copy_(a3[0])                     # written right before the next call reads it
+                fg.fg_gemm_fp8_nt(A3, a3[1], a3[2], a3[3], D3)
+                fg.fg_gemm_fp8_nt(*a1, D)
+            torch.cuda.synchronize()
+            results[pdl] = (d_to_bits(D), d_to_bits(D3))
+        finally:
+            fg.fg_set_programmatic_launch(True)
+    assert np.array_equal(results[False][0], results[True][0])
+    assert np.array_equal(results[False][1], results[True][1])
+    ref1, _ = oracle.gemm_fp8_nt(p1.A, 0, p1.sA, p1.B, 0, p1.sB, want_f64=False)
+    compare(results[True][0], ref1, what="last writer wins")
