@@ -106,11 +106,13 @@ struct SmemLayout {
     static constexpr int SA_OFF = STG_OFF + NUM_EPI_WARPS * STAGING_BYTES_PER_WARP;
     static constexpr int SB_OFF = SA_OFF + SCALE_STAGES * SA_STAGE_BYTES;
     static constexpr int BAR_OFF = SB_OFF + SCALE_STAGES * SB_STAGE_BYTES;
-    // full, empty, scale_full, scale_empty, tmem_full x2, tmem_empty x2, drain
-    static constexpr int NUM_BARS = 2 * STAGES + 2 * SCALE_STAGES + 4 + 1;
+    // TMEM: all 512 columns, as 512 / BN accumulator buffers of BN columns
+    static constexpr int TMEM_COLS = 512;
+    static constexpr int NUM_TBUF = TMEM_COLS / BN;
+    // full, empty, scale_full, scale_empty, tmem_full, tmem_empty, drain
+    static constexpr int NUM_BARS = 2 * STAGES + 2 * SCALE_STAGES + 2 * NUM_TBUF + 1;
     static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
     static constexpr int BYTES = MISC_OFF + 16;
-    static constexpr int TMEM_COLS = 2 * BN;
     // split-K partial tile (128 x BN FP32), aliased on the operand ring
     static constexpr int P_OFF = 0;
     static_assert(BLOCK_M * BN * 4 <= STG_OFF, "partial tile must fit in the operand ring");
@@ -266,6 +268,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     using L = SmemLayout<BN, STAGES>;
     constexpr int COLS = BN / 2;  // columns per promotion warp
     constexpr uint32_t STAGE_TX = A_STAGE_BYTES + L::B_STAGE_BYTES;
+    constexpr uint32_t NTB = L::NUM_TBUF;  // TMEM accumulator buffers (a power of two)
+    static_assert((NTB & (NTB - 1)) == 0 && NTB >= 2, "TMEM buffer count");
 
     extern __shared__ __align__(1024) uint8_t smem[];
     const uint32_t sbase = smem_u32(smem);
@@ -276,12 +280,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     auto sfull_bar = [&](uint32_t q) { return bar0 + 8u * (2 * STAGES + q); };
     auto sempty_bar = [&](uint32_t q) { return bar0 + 8u * (2 * STAGES + SCALE_STAGES + q); };
     auto tfull_bar = [&](uint32_t b) { return bar0 + 8u * (2 * STAGES + 2 * SCALE_STAGES + b); };
-    auto tempty_bar = [&](uint32_t b) { return bar0 + 8u * (2 * STAGES + 2 * SCALE_STAGES + 2 + b); };
-    const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 2 * SCALE_STAGES + 4);
+    auto tempty_bar = [&](uint32_t b) { return bar0 + 8u * (2 * STAGES + 2 * SCALE_STAGES + NTB + b); };
+    const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 2 * SCALE_STAGES + 2 * NTB);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::MISC_OFF);
     volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(smem + L::MISC_OFF + 4);
 
-    const int warp = threadIdx.x >> 5;
+    // warp index through a shuffle so the compiler knows it is warp-uniform
+    // (TMEM addresses derived from it then stay in uniform registers)
+    const int warp = __shfl_sync(0xffffffffu, (int)(threadIdx.x >> 5), 0);
     const int lane = threadIdx.x & 31;
 
     // The 128-byte swizzled TMA tiles need a 1024-byte aligned base.
@@ -308,7 +314,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 mbar_init(sfull_bar(q), 2);  // producer's expect_tx arrival + the cp.async arrival
                 mbar_init(sempty_bar(q), NUM_EPI_WARPS);
             }
-            for (int b = 0; b < 2; ++b) {
+            for (uint32_t b = 0; b < NTB; ++b) {
                 mbar_init(tfull_bar(b), 1);
                 mbar_init(tempty_bar(b), NUM_EPI_WARPS);
             }
@@ -420,7 +426,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 if (!ti.valid) continue;
                 for (int kb = kb_begin; kb < kb_end; ++kb, ++it) {
                     const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
-                    const uint32_t b = it & 1u, bph = (it >> 1) & 1u;
+                    const uint32_t b = it & (NTB - 1u), bph = (it / NTB) & 1u;
                     if (!wait_phase(tempty_bar(b), bph ^ 1u, abort_flag, p, ROLE_MMA) ||
                         !wait_phase(full_bar(s), ph, abort_flag, p, ROLE_MMA)) {
                         ok = false;
@@ -512,7 +518,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     for (int j = 0; j < TMEM_LD_COLS; j += 2)
                         ffma2(acc2[(c * TMEM_LD_COLS + j) / 2], v[j], v[j + 1], sc2);
                 }
-                b ^= 1u;
+                b = (b + 1u) & (NTB - 1u);
                 bph ^= (b == 0u);
                 q = (q + 1u) & (SCALE_STAGES - 1u);
                 qph ^= (q == 0u);
