@@ -16,22 +16,23 @@
 //               layout is MN-major) and the two RHS block scales by cp.async
 //               (`scale_full[q]`).
 //   warp 9      MMA issuer: one lane issues 4 tcgen05.mma (K = 32 each) per K
-//               block into one of two TMEM accumulators (128 lanes x BN
+//               block into one of 512/BN TMEM accumulators (128 lanes x BN
 //               columns, FP32), then commits to `empty[s]` (smem stage free)
 //               and `tmem_full[b]` (partial ready).
 //   warps 0..7  promotion + epilogue: warp w owns TMEM lanes 32*(w%4).. (its
 //               rows) and columns [(w/4)*BN/2, (w/4+1)*BN/2).  Per K block it
 //               reads its scales from the scale ring (releasing the entry), reads
-//               the partial with 32-column tcgen05.ld, hands the TMEM buffer back
+//               the partial in 32-column chunks of tcgen05.ld, hands the TMEM buffer back
 //               (`tmem_empty[b]`) as soon as the last load has landed, and adds
 //               sA*sB*partial into BN/2 FP32 registers per thread with packed
 //               fma.rn.f32x2.  After the last K block a warp converts its
 //               32 x BN/2 block to BF16, stages it in swizzled shared memory and
 //               writes it with TMA stores, or with per-row predicated stores
 //               when some of its rows must stay untouched (grouped layouts).
-// The two TMEM accumulators let the tensor cores run K block kb+1 while the
-// promotion warps consume K block kb, and run the next tile's first K blocks
-// while the epilogue of the previous tile drains.
+// The TMEM accumulators (two for BN = 256, four for BN = 128) let the tensor
+// cores run the next K blocks while the promotion warps consume K block kb,
+// and run the next tile's first K blocks while the previous tile's epilogue
+// drains.
 //
 // Split-K (SPLITK = true, for problems with fewer output tiles than SMs): the
 // grid is one cluster of S CTAs per output tile; CTA rank q runs K blocks
@@ -502,8 +503,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
                 for (int c = 0; c < COLS / TMEM_LD_COLS; ++c) {
                     uint32_t v[TMEM_LD_COLS];
-                    tmem_ld_32x32b_x16(taddr + c * TMEM_LD_COLS, *reinterpret_cast<uint32_t(*)[16]>(&v[0]));
-                    tmem_ld_32x32b_x16(taddr + c * TMEM_LD_COLS + 16, *reinterpret_cast<uint32_t(*)[16]>(&v[16]));
+#pragma unroll
+                    for (int u = 0; u < TMEM_LD_COLS / 8; ++u)
+                        tmem_ld_32x32b_x8(taddr + c * TMEM_LD_COLS + 8 * u, *reinterpret_cast<uint32_t(*)[8]>(&v[8 * u]));
                     tmem_ld_wait();
 #pragma unroll
                     for (int j = 0; j < TMEM_LD_COLS; ++j) reg_fence(v[j]);
