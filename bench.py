@@ -66,7 +66,9 @@ def sweep_problems():
     return probs, shapes
 
 
-def kernel_name(block_n, split):
+def kernel_name(block_n, split, pair=0):
+    if pair:
+        return "fg::fp8_gemm_pair_kernel<dense,5,8> (256x256 tiles on CTA pairs)"
     stages = 4 if block_n == 256 else 6
     return f"fg::fp8_gemm_kernel<{block_n},{stages},dense,{'splitk' if split > 1 else 'persistent'}>"
 
@@ -302,8 +304,8 @@ def run_ours(args, ws, rank, local):
     # group boundary gives every kernel's device time inside the timed region.
     groups = {}
     for i, (m, n, k, _) in enumerate(items):
-        bn, split = fg.fg_query_dense_plan(m, n, k)
-        groups.setdefault(kernel_name(bn, split), []).append(i)
+        bn, split, pair = fg.fg_query_dense_plan_ex(m, n, k)
+        groups.setdefault(kernel_name(bn, split, pair), []).append(i)
     group_names = list(groups)
     group_items = [groups[g] for g in group_names]
 
@@ -368,9 +370,10 @@ def run_ours(args, ws, rank, local):
                            "frac_hbm_peak": round(b / t / 1e9 / hbm_peak, 3),
                            "roofline_over_time": round(t_roof / t, 3)})
     for r in shape_rows:
-        bn, split = fg.fg_query_dense_plan(r["m"], r["n"], r["k"])
+        bn, split, pair = fg.fg_query_dense_plan_ex(r["m"], r["n"], r["k"])
         r["plan"] = {"block_n": bn, "split_k": split}
-        r["kernel"] = kernel_name(bn, split)
+        r["plan"]["cta_pair"] = pair
+        r["kernel"] = kernel_name(bn, split, pair)
     traffic_tab = load_traffic()
     ridge = fp8_peak * 1e12 / (hbm_peak * 1e9)
 

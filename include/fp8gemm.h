@@ -130,6 +130,20 @@ fg_status fg_set_config_override(int block_n, int split_k);
  * Host-only query (reads device attributes, launches nothing). */
 fg_status fg_query_dense_plan(int m, int n, int k, int *block_n, int *split_k);
 
+/* Same, plus whether the call runs on CTA pairs (*cta_pair = 1): 256 x 256
+ * output tiles shared by the two CTAs (two SMs) of a cluster, one
+ * tcgen05.mma.cta_group::2 per 32-deep K step, each CTA loading its 128 rows
+ * of A and its 128 of the tile's 256 rows of B.  The pages' design has no
+ * counterpart (Hopper has no paired tensor-core instruction). */
+fg_status fg_query_dense_plan_ex(int m, int n, int k, int *block_n, int *split_k, int *cta_pair);
+
+/* CTA-pair tiles for later calls: -1 (default) where they apply (persistent
+ * 256-wide plans of the dense and masked layouts with at least 256 rows, no
+ * forced plan), 0 never, 1 for every persistent 256-wide dense or masked plan.
+ * The contiguous layout always uses 128-row tiles.  Results differ between
+ * the modes only by FP32 summation order; FG_ERR_INVALID_ARG otherwise. */
+fg_status fg_set_pair_mode(int mode);
+
 /* Programmatic dependent launch of the GEMM kernels (default on): a call's
  * CTAs may start while the previous kernel of the stream finishes, set up
  * their shared memory, tensor memory and barriers, and wait for the previous

@@ -48,6 +48,8 @@ SIGNATURES = {
     "fg_set_config_override": (_I, [_I, _I]),
     "fg_set_programmatic_launch": (_I, [_I]),
     "fg_query_dense_plan": (_I, [_I, _I, _I, ctypes.POINTER(_I), ctypes.POINTER(_I)]),
+    "fg_query_dense_plan_ex": (_I, [_I, _I, _I, ctypes.POINTER(_I), ctypes.POINTER(_I), ctypes.POINTER(_I)]),
+    "fg_set_pair_mode": (_I, [_I]),
     "fg_status_string": (ctypes.c_char_p, [_I]),
     "fg_version": (_I, []),
     "fg_debug_skip_producer_iteration": (_I, [_I]),
@@ -222,6 +224,19 @@ def fg_query_dense_plan(m: int, n: int, k: int):
     bn, sp = ctypes.c_int(0), ctypes.c_int(0)
     _check("fg_query_dense_plan", lib().fg_query_dense_plan(int(m), int(n), int(k), ctypes.byref(bn), ctypes.byref(sp)))
     return bn.value, sp.value
+
+
+def fg_query_dense_plan_ex(m: int, n: int, k: int):
+    """(block_n, split_k, cta_pair) that a dense call of this shape would use."""
+    bn, sp, pr = ctypes.c_int(0), ctypes.c_int(0), ctypes.c_int(0)
+    _check("fg_query_dense_plan_ex", lib().fg_query_dense_plan_ex(int(m), int(n), int(k), ctypes.byref(bn),
+                                                                ctypes.byref(sp), ctypes.byref(pr)))
+    return bn.value, sp.value, pr.value
+
+
+def fg_set_pair_mode(mode: int) -> None:
+    """-1: CTA-pair tiles where they apply (default); 0: never; 1: every persistent 256-wide plan."""
+    _check("fg_set_pair_mode", lib().fg_set_pair_mode(int(mode)))
 
 
 def fg_set_programmatic_launch(enable: bool) -> None:

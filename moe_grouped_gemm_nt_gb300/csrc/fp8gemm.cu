@@ -13,6 +13,7 @@
 
 #include "../../include/fp8gemm.h"
 #include "gemm_kernel.cuh"
+#include "gemm_pair_kernel.cuh"
 
 namespace {
 
@@ -113,22 +114,23 @@ int cdiv(int a, int b) { return (a + b - 1) / b; }
 std::atomic<int> g_force_bn{0};
 std::atomic<int> g_pdl{1};  // programmatic dependent launch of the GEMM kernels
 std::atomic<int> g_force_split{0};
+std::atomic<int> g_pair_mode{-1};  // CTA-pair tiles: -1 where they apply, 0 never, 1 whenever allowed
 
-template <int BN, int STAGES, int KIND, bool SPLITK>
-struct Kernel {
-    using L = fg::SmemLayout<BN, STAGES>;
-
-    // launch configuration: a cluster dimension (split-K) and/or programmatic
-    // dependent launch (`at` holds room for two attributes)
+// Launch helper of one kernel instantiation F with BYTES of dynamic shared
+// memory; CLUSTERED kernels always carry a cluster dimension.
+template <auto F, int BYTES, bool CLUSTERED>
+struct Launcher {
+    // launch configuration: a cluster dimension and/or programmatic dependent
+    // launch (`at` holds room for two attributes)
     static cudaLaunchConfig_t config(int grid, int cluster, cudaStream_t stream, cudaLaunchAttribute *at,
                                      bool pdl = false) {
         cudaLaunchConfig_t cfg{};
         cfg.gridDim = dim3(grid, 1, 1);
         cfg.blockDim = dim3(fg::NUM_THREADS, 1, 1);
-        cfg.dynamicSmemBytes = L::BYTES;
+        cfg.dynamicSmemBytes = BYTES;
         cfg.stream = stream;
         unsigned n = 0;
-        if (cluster > 1 || SPLITK) {
+        if (cluster > 1 || CLUSTERED) {
             at[n].id = cudaLaunchAttributeClusterDimension;
             at[n].val.clusterDim.x = cluster;
             at[n].val.clusterDim.y = 1;
@@ -152,8 +154,7 @@ struct Kernel {
         if (cudaGetDevice(&dev) != cudaSuccess) return false;
         const uint64_t bit = 1ull << (dev & 63);
         if (configured.load(std::memory_order_acquire) & bit) return true;
-        if (cudaFuncSetAttribute(fg::fp8_gemm_kernel<BN, STAGES, KIND, SPLITK>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, L::BYTES) != cudaSuccess)
+        if (cudaFuncSetAttribute(F, cudaFuncAttributeMaxDynamicSharedMemorySize, BYTES) != cudaSuccess)
             return false;
         configured.fetch_or(bit, std::memory_order_acq_rel);
         return true;
@@ -170,8 +171,7 @@ struct Kernel {
         cudaLaunchAttribute at[2];
         cudaLaunchConfig_t cfg = config(cluster, cluster, nullptr, at);
         int n = 0;
-        if (cudaOccupancyMaxActiveClusters(&n, fg::fp8_gemm_kernel<BN, STAGES, KIND, SPLITK>, &cfg) !=
-            cudaSuccess) {
+        if (cudaOccupancyMaxActiveClusters(&n, F, &cfg) != cudaSuccess) {
             cudaGetLastError();
             return 0;
         }
@@ -185,11 +185,21 @@ struct Kernel {
         if (!configure()) return cuda_fail();
         cudaLaunchAttribute at[2];
         cudaLaunchConfig_t cfg = config(grid, cluster, stream, at, g_pdl.load() != 0);
-        if (cudaLaunchKernelEx(&cfg, fg::fp8_gemm_kernel<BN, STAGES, KIND, SPLITK>, ta, tb, td, tsa, p) != cudaSuccess)
-            return cuda_fail();
+        if (cudaLaunchKernelEx(&cfg, F, ta, tb, td, tsa, p) != cudaSuccess) return cuda_fail();
         return cudaPeekAtLastError() == cudaSuccess ? FG_OK : cuda_fail();
     }
 };
+
+template <int BN, int STAGES, int KIND, bool SPLITK>
+using Kernel = Launcher<fg::fp8_gemm_kernel<BN, STAGES, KIND, SPLITK>, fg::SmemLayout<BN, STAGES>::BYTES, SPLITK>;
+
+// 256 x 256 tiles on CTA pairs: operand stages of 16 + 16 KB per CTA, and a
+// scale ring at least as deep (the producer issues both in the same iteration)
+constexpr int kPairStages = 5;
+constexpr int kPairScaleStages = 8;
+template <int KIND>
+using PairKernel = Launcher<fg::fp8_gemm_pair_kernel<KIND, kPairStages, kPairScaleStages>,
+                            fg::PairSmemLayout<kPairStages, kPairScaleStages>::BYTES, true>;
 
 // Tile plan of one call: output tile width and split-K factor.
 struct Plan {
@@ -279,6 +289,20 @@ int raster_group_m(int kind, int m_blocks, int k) {
     return (int)(g > 0 ? g : 1);
 }
 
+// Whether a call runs on CTA pairs (256 x 256 tiles): persistent 256-wide plans
+// of the dense and masked layouts with at least 256 rows (per group), unless
+// a tile plan is forced or the pair mode says otherwise.  The contiguous
+// layout keeps 128-row tiles: two adjacent 128-row blocks may belong to
+// different groups, which one pair MMA (one B) cannot serve.
+bool use_pair(int kind, const Plan &plan, int rows) {
+    if (kind == fg::KIND_CONTIGUOUS || plan.split != 1 || plan.bn != 256) return false;
+    const int mode = g_pair_mode.load();
+    if (mode == 0) return false;
+    if (mode == 1) return true;
+    if (g_force_bn.load() != 0 || g_force_split.load() != 0) return false;
+    return rows >= fg::PAIR_ROWS;
+}
+
 // Shared part of the three GEMM entry points.
 //   a_rows: rows of the 2-D A / D row space; b_rows: G * n.
 template <int KIND>
@@ -310,13 +334,14 @@ fg_status run(const void *A, int a_fmt, const float *sA, int ld_sA, const void *
     const long long m_blocks_total = (long long)cdiv(rows, fg::BLOCK_M) * (KIND == fg::KIND_MASKED ? G : 1);
     const Plan plan = choose_plan(m_blocks_total, KIND == fg::KIND_DENSE ? rows : INT32_MAX, n, k, sms);
     const int BN = plan.bn;
+    const bool pair = use_pair(KIND, plan, rows);
 
     CUtensorMap ta, tb, td, tsa;
     if (!encode_scales_a(&tsa, sA, ld_sA, rows, cdiv(k, fg::BLOCK_K), G, KIND == fg::KIND_MASKED) ||
         !encode_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, (uint64_t)k, (uint64_t)a_rows_total, (uint64_t)k,
                    fg::BLOCK_K, fg::BLOCK_M) ||
         !encode_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, (uint64_t)k, (uint64_t)G * n, (uint64_t)k, fg::BLOCK_K,
-                   (uint32_t)BN) ||
+                   (uint32_t)(pair ? fg::PAIR_BN / 2 : BN)) ||
         !encode_2d(&td, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, D, (uint64_t)n, (uint64_t)a_rows_total,
                    (uint64_t)n * 2, 64, 32))
         return cuda_fail();
@@ -340,6 +365,21 @@ fg_status run(const void *A, int a_fmt, const float *sA, int ld_sA, const void *
     p.timeout_ns = (unsigned long long)g_watchdog_ms.load() * 1000000ull;
     p.debug_skip_iter = g_debug_skip_iter.exchange(-1);
 
+    if constexpr (KIND != fg::KIND_CONTIGUOUS) {
+        if (pair) {
+            // 256 x 256 tiles on CTA pairs: the raster counts 256-row blocks
+            // (whose A rows take twice the bytes of a 128-row block)
+            const long long pblocks = (long long)cdiv(rows, fg::PAIR_ROWS) * (KIND == fg::KIND_MASKED ? G : 1);
+            p.num_n_blocks = cdiv(n, fg::PAIR_BN);
+            p.group_m = raster_group_m(KIND, (int)pblocks, 2 * k);
+            p.idesc = fg::make_idesc_f8f6f4(fg::PAIR_ROWS, fg::PAIR_BN, (uint32_t)a_fmt, (uint32_t)b_fmt);
+            const long long tiles = pblocks * p.num_n_blocks;
+            long long clusters = PairKernel<KIND>::max_active_clusters(2);
+            if (clusters < 1) return cuda_fail();
+            if (clusters > tiles) clusters = tiles;
+            return PairKernel<KIND>::launch(ta, tb, td, tsa, p, (int)(2 * clusters), 2, stream);
+        }
+    }
     const long long max_tiles = m_blocks_total * p.num_n_blocks;
     {
         if (plan.split > 1) {
@@ -423,6 +463,23 @@ fg_status fg_query_dense_plan(int m, int n, int k, int *block_n, int *split_k) {
     const Plan plan = choose_plan(cdiv(m, fg::BLOCK_M), m, n, k, sms);
     *block_n = plan.bn;
     *split_k = plan.split;
+    return FG_OK;
+}
+
+fg_status fg_query_dense_plan_ex(int m, int n, int k, int *block_n, int *split_k, int *cta_pair) {
+    if (!cta_pair) return FG_ERR_INVALID_ARG;
+    const fg_status st = fg_query_dense_plan(m, n, k, block_n, split_k);
+    if (st != FG_OK) return st;
+    Plan plan;
+    plan.bn = *block_n;
+    plan.split = *split_k;
+    *cta_pair = use_pair(fg::KIND_DENSE, plan, m) ? 1 : 0;
+    return FG_OK;
+}
+
+fg_status fg_set_pair_mode(int mode) {
+    if (mode < -1 || mode > 1) return FG_ERR_INVALID_ARG;
+    g_pair_mode.store(mode);
     return FG_OK;
 }
 

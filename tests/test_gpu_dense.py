@@ -204,3 +204,48 @@ def test_programmatic_launch_keeps_stream_order():
     assert np.array_equal(results[False][1], results[True][1])
     ref1, _ = oracle.gemm_fp8_nt(p1.A, 0, p1.sA, p1.B, 0, p1.sB, want_f64=False)
     compare(results[True][0], ref1, what="last writer wins")
+
+
+# ------------------------------------------------------------- CTA pairs
+
+@pytest.fixture
+def pair_mode():
+    import moe_grouped_gemm_nt_gb300 as fg
+
+    yield fg.fg_set_pair_mode
+    fg.fg_set_pair_mode(-1)
+
+
+@pytest.mark.parametrize("m,n,k", [(256, 512, 640), (300, 264, 1040), (384, 520, 384), (1, 256, 128),
+                                   (640, 2112, 272), (1030, 1800, 1536)])
+def test_pair_tiles_match_oracle(pair_mode, m, n, k):
+    """256 x 256 tiles on CTA pairs (forced for every persistent 256-wide plan,
+    including m < 256 where the odd CTA's half is empty): full comparison,
+    partial M, N and K tiles included."""
+    import moe_grouped_gemm_nt_gb300 as fg
+
+    pair_mode(1)
+    bn, split, pair = fg.fg_query_dense_plan_ex(m, n, k)
+    p = wl.dense(m, n, k, seed=9100 + m + n + k)
+    _full_check(p, f"dense pair {m}x{n}x{k} (plan {bn},{split},{pair})")
+
+
+def test_pair_and_single_cta_tiles_agree(pair_mode):
+    """The same problem on CTA pairs and on one-CTA tiles: both within the
+    oracle tolerance, and repeated pair calls bitwise equal."""
+    p = wl.dense(1024, 2048, 2048, seed=9201)
+    ref16, _ = oracle.gemm_fp8_nt(p.A, 0, p.sA, p.B, 0, p.sB, want_f64=False)
+    pair_mode(1)
+    a = d_to_bits(run_dense(p))
+    assert np.array_equal(a, d_to_bits(run_dense(p)))
+    pair_mode(0)
+    b = d_to_bits(run_dense(p))
+    compare(a, ref16, what="pair")
+    compare(b, ref16, what="single")
+
+
+def test_pair_plan_query():
+    import moe_grouped_gemm_nt_gb300 as fg
+
+    assert fg.fg_query_dense_plan_ex(4096, 7168, 2048)[2] == 1
+    assert fg.fg_query_dense_plan_ex(128, 7168, 2048)[2] == 0

@@ -120,6 +120,24 @@ def test_masked_small_full(counts, M_cap, n, k):
         compare(got[valid], ref[valid], what=f"masked {counts}")
 
 
+@pytest.mark.parametrize("pair", [0, 1])
+@pytest.mark.parametrize("counts,M_cap", [([0, 1, 255, 256, 257, 384, 512], 512), ([130, 300], 384)])
+def test_masked_pair_tiles(counts, M_cap, pair):
+    """Masked layout on CTA pairs (256-row blocks inside a group) and on
+    one-CTA tiles: rows past each count untouched, the rest within tolerance."""
+    fg.fg_set_pair_mode(pair)
+    try:
+        p = wl.masked(len(counts), M_cap, n=520, k=384, seed=M_cap + 11 * pair, masked_m=counts)
+        got = d_to_bits(run_masked(p))
+    finally:
+        fg.fg_set_pair_mode(-1)
+    init = np.full((p.G, p.M_cap, p.n), SENTINEL, np.uint16)
+    ref, _ = oracle.grouped_masked(p.A, 0, p.sA, p.B, 0, p.sB, p.masked_m, init)
+    valid = np.arange(M_cap)[None, :] < np.clip(p.masked_m, 0, M_cap)[:, None]
+    assert np.array_equal(got[~valid], ref[~valid]), "rows past the count were written"
+    compare(got[valid], ref[valid], what=f"masked pair={pair} {counts}")
+
+
 def run_masked_allow_check(p, expect_check):
     if not expect_check:
         return run_masked(p)
