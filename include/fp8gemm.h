@@ -140,8 +140,10 @@ fg_status fg_query_dense_plan_ex(int m, int n, int k, int *block_n, int *split_k
 /* CTA-pair tiles for later calls: -1 (default) where they apply (persistent
  * 256-wide plans of the dense and masked layouts with at least 256 rows, no
  * forced plan), 0 never, 1 for every persistent 256-wide dense or masked plan.
- * The contiguous layout always uses 128-row tiles.  Results differ between
- * the modes only by FP32 summation order; FG_ERR_INVALID_ARG otherwise. */
+ * The contiguous layout always uses 128-row tiles (two adjacent 128-row blocks
+ * may belong to two groups; measured, pairing them with a second pass for
+ * such blocks was slower than 128-row tiles).  Results differ between the
+ * modes only by FP32 summation order; FG_ERR_INVALID_ARG for other values. */
 fg_status fg_set_pair_mode(int mode);
 
 /* Programmatic dependent launch of the GEMM kernels (default on): a call's

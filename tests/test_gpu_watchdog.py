@@ -19,13 +19,16 @@ if not torch.cuda.is_available():
 from gpu_common import compare, d_to_bits, dev, fp8_dtype, run_dense  # noqa: E402
 
 
-@pytest.fixture
-def short_watchdog():
+@pytest.fixture(params=[0, 1], ids=["one_cta", "cta_pair"])
+def short_watchdog(request):
+    """Persistent 128x256 tiles on one CTA, or 256x256 tiles on CTA pairs."""
     fg.fg_set_watchdog_ms(200)
     fg.fg_set_config_override(256, 1)
+    fg.fg_set_pair_mode(request.param)
     yield
     fg.fg_set_watchdog_ms(0)
     fg.fg_set_config_override(0, 0)
+    fg.fg_set_pair_mode(-1)
     fg.lib().fg_debug_skip_producer_iteration(-1)
 
 
