@@ -606,7 +606,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     constexpr int CH = BN / 4;  // 16-byte chunks per partial row
                     constexpr int MAX_SPLIT = 8;
                     constexpr int STRIDE = NUM_EPI_WARPS * 32;
-                    const int r0 = (int)((BLOCK_M * rank) / split), r1 = (int)((BLOCK_M * (rank + 1)) / split);
+                    // rows of the tile that are written, shared evenly by the ranks
+                    // (contiguous: all 128, the per-row group test below decides)
+                    const int nrows = KIND == KIND_CONTIGUOUS ? BLOCK_M : max(0, min(BLOCK_M, ti.row_limit));
+                    const int r0 = (int)((nrows * rank) / split), r1 = (int)((nrows * (rank + 1)) / split);
                     const int col_base = ti.n_blk * BN;
                     const int items = (r1 - r0) * CH;
                     // two chunks per thread per pass, all ranks' loads issued before any
