@@ -76,3 +76,19 @@ def test_grouped_argument_checks():
                                         None) == 1
     assert L.fg_scales_a_to_mn_major(FAKE, FAKE, 1, 10, 2, 10, None) == 2
     assert L.fg_scales_a_to_mn_major(FAKE, FAKE, 1, 10, 2, 8, None) == 1
+
+
+def test_tuning_knob_argument_checks():
+    """The plan and pair-mode knobs validate their arguments on the host."""
+    h = fg.lib()
+    for mode in (-2, 2, 7):
+        assert h.fg_set_pair_mode(mode) == 1
+    for mode in (-1, 0, 1):
+        assert h.fg_set_pair_mode(mode) == 0
+    h.fg_set_pair_mode(-1)
+    for bn, split in ((64, 1), (256, 9), (128, -1)):
+        assert h.fg_set_config_override(bn, split) == 1
+    assert h.fg_set_config_override(0, 0) == 0
+    out = ctypes.c_int(0)
+    assert h.fg_query_dense_plan_ex(128, 256, 512, ctypes.byref(out), ctypes.byref(out), None) == 1
+    assert h.fg_query_dense_plan(0, 256, 512, ctypes.byref(out), ctypes.byref(out)) == 1
