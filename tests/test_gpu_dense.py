@@ -249,3 +249,20 @@ def test_pair_plan_query():
 
     assert fg.fg_query_dense_plan_ex(4096, 7168, 2048)[2] == 1
     assert fg.fg_query_dense_plan_ex(128, 7168, 2048)[2] == 0
+
+
+@pytest.mark.parametrize("mode,bn,split", [("pair", 0, 0), ("one_cta", 256, 1), ("split", 128, 4)])
+def test_repeat_20x_bitwise(pair_mode, plan_override, mode, bn, split):
+    """Twenty identical calls give identical bits (a race in a pipeline, a
+    barrier phase or the split-K exchange would show up as run-to-run noise)."""
+    if mode == "pair":
+        pair_mode(1)
+    else:
+        pair_mode(0)
+        plan_override(bn, split)
+    p = wl.dense(768 if mode != "split" else 128, 2112, 3072, seed=9300 + bn + split)
+    first = d_to_bits(run_dense(p))
+    for _ in range(19):
+        assert np.array_equal(first, d_to_bits(run_dense(p))), mode
+    ref16, _ = oracle.gemm_fp8_nt(p.A, 0, p.sA, p.B, 0, p.sB, want_f64=False)
+    compare(first, ref16, what=f"repeat {mode}")
