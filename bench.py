@@ -74,14 +74,21 @@ def kernel_name(block_n, split, pair=0):
 
 
 def kernel_sources_digest():
-    """Digest of the CUDA sources: DRAM traffic figures are only used when
-    they were captured on the kernels built from these exact sources."""
+    """Digest of the CUDA sources with comments removed and white space
+    collapsed: DRAM traffic figures are only used when they were captured on
+    kernels built from the same code."""
     import hashlib
+    import re
     h = hashlib.sha1()
     d = os.path.join(ROOT, "moe_grouped_gemm_nt_gb300", "csrc")
     for f in sorted(os.listdir(d)):
-        with open(os.path.join(d, f), "rb") as fh:
-            h.update(f.encode() + fh.read())
+        with open(os.path.join(d, f), encoding="utf-8") as fh:
+            text = fh.read()
+        # drop comments (string literals in these sources hold no comment markers)
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        text = re.sub(r"\s+", " ", text)
+        h.update(f.encode() + text.encode())
     return h.hexdigest()[:16]
 
 

@@ -8,7 +8,9 @@
 //   * CTA rank r holds rows [r*128, r*128+128) of the tile's A block and rows
 //     [r*128, r*128+128) of the tile's 256 B rows, so each SM brings in 32 KB
 //     per K block instead of 48 KB for a 128 x 256 tile; the same shared memory
-//     then holds six stages instead of four.
+//     then holds more stages (five, with an eight-deep scale ring: the
+//     producer issues both in the same iteration, so its lookahead is the
+//     shallower of the two).
 //   * The even CTA's MMA warp issues tcgen05.mma.cta_group::2 (M = 256,
 //     N = 256, K = 32); each CTA's TMEM receives its 128 rows x 256 columns.
 //     Both CTAs' operand loads signal the even CTA's `full[s]`; its commits
