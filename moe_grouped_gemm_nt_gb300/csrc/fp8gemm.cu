@@ -334,7 +334,7 @@ fg_status run(const void *A, int a_fmt, const float *sA, int ld_sA, const void *
     const long long m_blocks_total = (long long)cdiv(rows, fg::BLOCK_M) * (KIND == fg::KIND_MASKED ? G : 1);
     const Plan plan = choose_plan(m_blocks_total, KIND == fg::KIND_DENSE ? rows : INT32_MAX, n, k, sms);
     const int BN = plan.bn;
-    const bool pair = use_pair(KIND, plan, rows);
+    const bool pair = use_pair(KIND, plan, rows) && sms >= 2;
 
     CUtensorMap ta, tb, td, tsa;
     if (!encode_scales_a(&tsa, sA, ld_sA, rows, cdiv(k, fg::BLOCK_K), G, KIND == fg::KIND_MASKED) ||
@@ -376,6 +376,7 @@ fg_status run(const void *A, int a_fmt, const float *sA, int ld_sA, const void *
             const long long tiles = pblocks * p.num_n_blocks;
             long long clusters = PairKernel<KIND>::max_active_clusters(2);
             if (clusters < 1) return cuda_fail();
+            if (clusters > sms / 2) clusters = sms / 2;  // the SM limit (fg_set_num_sms); sms >= 2 here
             if (clusters > tiles) clusters = tiles;
             return PairKernel<KIND>::launch(ta, tb, td, tsa, p, (int)(2 * clusters), 2, stream);
         }
@@ -473,7 +474,7 @@ fg_status fg_query_dense_plan_ex(int m, int n, int k, int *block_n, int *split_k
     Plan plan;
     plan.bn = *block_n;
     plan.split = *split_k;
-    *cta_pair = use_pair(fg::KIND_DENSE, plan, m) ? 1 : 0;
+    *cta_pair = use_pair(fg::KIND_DENSE, plan, m) && g_num_sms_override.load() != 1 ? 1 : 0;
     return FG_OK;
 }
 

@@ -266,3 +266,20 @@ def test_repeat_20x_bitwise(pair_mode, plan_override, mode, bn, split):
         assert np.array_equal(first, d_to_bits(run_dense(p))), mode
     ref16, _ = oracle.gemm_fp8_nt(p.A, 0, p.sA, p.B, 0, p.sB, want_f64=False)
     compare(first, ref16, what=f"repeat {mode}")
+
+
+@pytest.mark.parametrize("num_sms", [1, 2, 16, 77])
+def test_sm_limit(pair_mode, num_sms):
+    """fg_set_num_sms caps the persistent grid (one-CTA and CTA-pair tiles);
+    the results stay exact."""
+    import moe_grouped_gemm_nt_gb300 as fg
+
+    p = wl.dense(640, 1040, 1024, seed=9400 + num_sms)
+    ref16, _ = oracle.gemm_fp8_nt(p.A, 0, p.sA, p.B, 0, p.sB, want_f64=False)
+    fg.fg_set_num_sms(num_sms)
+    try:
+        for mode in (0, 1):
+            pair_mode(mode)
+            compare(d_to_bits(run_dense(p)), ref16, what=f"sms={num_sms} pair={mode}")
+    finally:
+        fg.fg_set_num_sms(0)
