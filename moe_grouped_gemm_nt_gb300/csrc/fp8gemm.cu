@@ -261,6 +261,7 @@ Plan choose_plan(long long m_blocks, int rows, int n, int k, int sms) {
                 const int clusters = bn == 256 ? Kernel<256, 4, fg::KIND_DENSE, true>::max_active_clusters(sp)
                                                : Kernel<128, 6, fg::KIND_DENSE, true>::max_active_clusters(sp);
                 cap = (long long)sp * clusters;
+                if (cap > (long long)(sms / sp) * sp) cap = (long long)(sms / sp) * sp;  // the SM limit
                 // a second wave of clusters would pay start-up and exchange again
                 if (cap <= 0 || m_blocks * cdiv(n, bn) * sp > cap) continue;
             }

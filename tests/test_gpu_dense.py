@@ -268,13 +268,14 @@ def test_repeat_20x_bitwise(pair_mode, plan_override, mode, bn, split):
     compare(first, ref16, what=f"repeat {mode}")
 
 
+@pytest.mark.parametrize("m", [640, 128])
 @pytest.mark.parametrize("num_sms", [1, 2, 16, 77])
-def test_sm_limit(pair_mode, num_sms):
-    """fg_set_num_sms caps the persistent grid (one-CTA and CTA-pair tiles);
-    the results stay exact."""
+def test_sm_limit(pair_mode, num_sms, m):
+    """fg_set_num_sms caps the grid (persistent one-CTA and CTA-pair tiles;
+    split-K plans only where they fit the limit); the results stay exact."""
     import moe_grouped_gemm_nt_gb300 as fg
 
-    p = wl.dense(640, 1040, 1024, seed=9400 + num_sms)
+    p = wl.dense(m, 1040, 1024, seed=9400 + num_sms + m)
     ref16, _ = oracle.gemm_fp8_nt(p.A, 0, p.sA, p.B, 0, p.sB, want_f64=False)
     fg.fg_set_num_sms(num_sms)
     try:
