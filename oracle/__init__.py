@@ -15,6 +15,10 @@ the header of ``oracle.c``:
 * ``grouped_contiguous``     -- same page, "连续布局分组GEMM".
 * ``grouped_masked``         -- same page, "掩码布局分组GEMM".
 * ``decode`` / ``bf16_rne``  -- FP8 decoding and FP64 -> bfloat16 rounding.
+* ``encode_fp8``             -- float32 -> FP8 code, nearest even, saturating.
+* ``quantize_per_token``     -- 1x128 activation quantization producing the
+  GEMM's LHS and its scales (same page, "基本用法"; page "企业官网建设流程全解析",
+  section 5.2).
 * ``*_at`` variants          -- the same definitions at sampled positions.
 
 Every function is pinned by ``tests/test_oracle_pins.py``.
@@ -79,6 +83,10 @@ def _load():
         lib.oracle_grouped_masked.argtypes = [P, I, P, P, I, P, P, I, I, I, I, P, P]
         lib.oracle_grouped_masked_at.restype = I
         lib.oracle_grouped_masked_at.argtypes = [P, I, P, P, I, P, P, I, I, I, I, LL, P, P, P, P, P]
+        lib.oracle_encode_fp8.restype = I
+        lib.oracle_encode_fp8.argtypes = [I, ctypes.c_float]
+        lib.oracle_quantize_per_token.restype = I
+        lib.oracle_quantize_per_token.argtypes = [P, I, I, P, P, I, I]
         lib.oracle_num_threads.restype = I
         lib.oracle_num_threads.argtypes = []
         lib.oracle_set_num_threads.restype = None
@@ -130,6 +138,30 @@ def decode_table(fmt: int) -> np.ndarray:
 def bf16_rne(x: float) -> int:
     """bfloat16 bit pattern of x rounded to nearest, ties to even, from FP64."""
     return int(_load().oracle_bf16_rne(float(x)))
+
+
+def encode_fp8(fmt: int, v: float) -> int:
+    """FP8 code of the float32 value v: nearest, ties to even, saturating."""
+    return int(_load().oracle_encode_fp8(int(fmt), float(np.float32(v))))
+
+
+def quantize_per_token(x, fmt: int):
+    """Per 1x128 row-group quantization of x [..., rows, k] (float32; bfloat16
+    values widen exactly).  Returns (q uint8 [..., rows, k], s float32
+    [..., rows, ceil(k/128)] row-major)."""
+    x = _f32(x)
+    *lead, rows, k = x.shape
+    kb = _num_kb(k)
+    nb = int(np.prod(lead)) if lead else 1
+    flat = x.reshape(nb, rows, k)
+    q = np.empty((flat.shape[0], rows, k), np.uint8)
+    s = np.empty((flat.shape[0], rows, kb), np.float32)
+    lib = _load()
+    for b in range(flat.shape[0]):
+        xb = np.ascontiguousarray(flat[b])
+        if lib.oracle_quantize_per_token(_ptr(xb), k, int(fmt), _ptr(q[b]), _ptr(s[b]), rows, k) != 0:
+            raise ValueError("oracle_quantize_per_token: bad argument")
+    return q.reshape(*lead, rows, k), s.reshape(*lead, rows, kb)
 
 
 def _num_kb(k):

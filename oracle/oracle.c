@@ -23,6 +23,13 @@
  * shorter), dec() decodes an FP8 byte to its real value, and bf16_rne rounds the
  * FP64 value directly to bfloat16, ties to even.
  *
+ * The same file states the step before the GEMM: per-token (1 x 128)
+ * quantization of activations into the FP8 LHS and its scales
+ * (oracle_quantize_per_token, with the FP8 encoder oracle_encode_fp8), from
+ * the same page's section "基本用法" and section 5.2 of the page
+ * "企业官网建设流程全解析" (scales come from a scan for each group's
+ * largest magnitude).
+ *
  * Pins: every function here is checked by tests/test_oracle_pins.py against
  * values fixed by the pages (format widths and maxima of E4M3/E5M2, page
  * "DeepGEMM：基于 Hopper Tensor Core 的 FP8 矩阵乘法内核优化实践" section 3.1 table), closed forms, brute force
@@ -326,6 +333,93 @@ int oracle_grouped_masked_at(const uint8_t *A, int a_fmt, const float *sA,
                                       k, ta, tb);
             if (D64) D64[i] = v;
             if (D16) D16[i] = oracle_bf16_rne(v);
+        }
+    }
+    return 0;
+}
+
+/* ------------------------------------------- per-token FP8 quantization */
+
+/* FP8 code of the float v rounded to nearest, ties to even, saturating at the
+ * largest finite magnitude (448 for E4M3, 57344 for E5M2; page
+ * "DeepGEMM：基于 Hopper Tensor Core 的 FP8 矩阵乘法内核优化实践", section 3.1).
+ * Written from the definition of rounding: among the finite non-negative codes,
+ * whose values grow with the code, take the two that bracket |v| and keep the
+ * nearer; on a tie keep the one whose last mantissa bit (the code's bit 0) is
+ * 0.  The sign bit is v's sign bit (so -0 and negative values that round to
+ * zero give 0x80).  v must be finite; NaN gives 0xFF. */
+static int encode_in_table(const double table[256], int top, float v) {
+    double a;
+    int lo, hi;
+    unsigned sign;
+    if (isnan(v)) return 0xFF;
+    sign = signbit(v) ? 0x80u : 0u;
+    a = fabs((double)v);
+    if (a >= table[top]) return (int)(sign | (unsigned)top);
+    /* table[lo] <= a < table[hi], hi = lo + 1 (binary search, codes 0..top) */
+    lo = 0;
+    hi = top;
+    while (hi - lo > 1) {
+        int mid = (lo + hi) / 2;
+        if (table[mid] <= a) lo = mid; else hi = mid;
+    }
+    {
+        double dlo = a - table[lo], dhi = table[hi] - a;
+        int c = dlo < dhi ? lo : dhi < dlo ? hi : ((lo & 1) == 0 ? lo : hi);
+        return (int)(sign | (unsigned)c);
+    }
+}
+
+static int top_code(int fmt) { return fmt == ORACLE_E4M3 ? 0x7E : 0x7B; } /* largest finite positive code */
+
+int oracle_encode_fp8(int fmt, float v) {
+    double table[256];
+    if (fill_table(fmt, table) != 0) return -1;
+    return encode_in_table(table, top_code(fmt), v);
+}
+
+/* Per-token (1 x 128) quantization of activations, the step that produces the
+ * LHS of the GEMM: page "DeepSeek开源周第三天DeepGEMM", section "基本用法" (the
+ * LHS is FP8 with one FP32 scale per row and 128-wide K block), and page
+ * "企业官网建设流程全解析", section 5.2 (a scale is found by scanning the
+ * group for its largest magnitude).  For each row r and K block kb, over the
+ * columns of the block that lie inside k:
+ *
+ *   amax      = max |x[r][c]|
+ *   s[r][kb]  = amax / fmax      (float32 division; 1 when amax == 0, so an
+ *                                 all-zero group never divides by zero)
+ *   q[r][c]   = encode( x[r][c] / s[r][kb] )   (float32 division, then the
+ *                                               rounding of oracle_encode_fp8)
+ *
+ * Every step is float32 because the codes are integers decided by floating
+ * point: the quantizer being checked decides them in float32 as well.
+ * x is float [rows][ld_x] (bfloat16 inputs widen to float exactly), q is
+ * [rows][k] bytes, s is row-major [rows][ceil(k/128)].  Returns 0, or -1 for
+ * a bad argument. */
+int oracle_quantize_per_token(const float *x, int ld_x, int fmt, uint8_t *q, float *s, int rows, int k) {
+    double table[256];
+    int kb, top;
+    float fmax;
+    if (fill_table(fmt, table) != 0) return -1;
+    if (rows < 0 || k < 1 || ld_x < k) return -1;
+    top = top_code(fmt);
+    fmax = fmt == ORACLE_E4M3 ? 448.0f : 57344.0f;
+    kb = (k + ORACLE_KBLOCK - 1) / ORACLE_KBLOCK;
+#pragma omp parallel for schedule(static)
+    for (int r = 0; r < rows; ++r) {
+        for (int b = 0; b < kb; ++b) {
+            int c0 = b * ORACLE_KBLOCK;
+            int c1 = c0 + ORACLE_KBLOCK < k ? c0 + ORACLE_KBLOCK : k;
+            const float *xr = x + (size_t)r * (size_t)ld_x;
+            float amax = 0.0f, scale;
+            for (int c = c0; c < c1; ++c) {
+                float m = fabsf(xr[c]);
+                if (m > amax) amax = m;
+            }
+            scale = amax > 0.0f ? amax / fmax : 1.0f;
+            s[(size_t)r * (size_t)kb + (size_t)b] = scale;
+            for (int c = c0; c < c1; ++c)
+                q[(size_t)r * (size_t)k + (size_t)c] = (uint8_t)encode_in_table(table, top, xr[c] / scale);
         }
     }
     return 0;

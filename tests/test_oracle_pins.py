@@ -401,3 +401,152 @@ def test_oracle_rejects_bad_shapes():
     with pytest.raises(ValueError):
         oracle.gemm_fp8_nt(A, 0, np.zeros((2, 0), np.float32), np.zeros((2, 0), np.uint8), 0,
                            np.zeros((1, 0), np.float32))
+
+
+# ------------------------------------------- per-token FP8 quantization
+#
+# The quantizer's two parts are pinned separately: the float32 -> FP8 encoder
+# by hand-worked codes, by torch's float8 conversion and by a brute-force
+# nearest-code search written here; the 1x128 group steps (largest magnitude,
+# scale = amax / fmax, division) by the input generator's numpy + torch
+# quantizer, by brute force on tiny rows and by closed forms.
+
+FMAX = {oracle.E4M3: 448.0, oracle.E5M2: 57344.0}
+
+
+@pytest.mark.parametrize("fmt,v,code", [
+    # E4M3: 1 sign, 4 exponent (bias 7), 3 mantissa bits
+    (oracle.E4M3, 1.5, 0x3C), (oracle.E4M3, -1.5, 0xBC), (oracle.E4M3, 448.0, 0x7E),
+    (oracle.E4M3, 500.0, 0x7E), (oracle.E4M3, 1e30, 0x7E), (oracle.E4M3, -1e30, 0xFE),
+    (oracle.E4M3, 2.0 ** -9, 0x01),
+    (oracle.E4M3, 2.0 ** -10, 0x00),        # tie between 0 and the smallest subnormal: even
+    (oracle.E4M3, 3 * 2.0 ** -10, 0x02),    # tie between 0x01 and 0x02: even
+    (oracle.E4M3, 1.0625, 0x38),            # tie between 1.0 and 1.125: even (1.0)
+    (oracle.E4M3, 1.1875, 0x3A),            # tie between 1.125 and 1.25: even (1.25)
+    (oracle.E4M3, 1.0625 + 2.0 ** -20, 0x39),  # just above the tie
+    (oracle.E4M3, -0.0, 0x80), (oracle.E4M3, 0.0, 0x00), (oracle.E4M3, -1e-10, 0x80),
+    # E5M2: 1 sign, 5 exponent (bias 15), 2 mantissa bits
+    (oracle.E5M2, 1.5, 0x3E), (oracle.E5M2, 57344.0, 0x7B), (oracle.E5M2, 1e9, 0x7B),
+    (oracle.E5M2, 2.0 ** -16, 0x01), (oracle.E5M2, 1.125, 0x3C), (oracle.E5M2, 1.375, 0x3E),
+    (oracle.E5M2, -2.0 ** -17, 0x80),       # tie between -0 and -2^-16: even
+])
+def test_encode_hand_worked(fmt, v, code):
+    assert oracle.encode_fp8(fmt, v) == code
+
+
+def _encode_brute(fmt, v):
+    """Nearest finite code by scanning all codes of v's sign (rounding is
+    symmetric, so the sign bit is v's); ties to the even code; beyond the
+    largest finite magnitude, that magnitude."""
+    t = oracle.decode_table(fmt)
+    v = float(np.float32(v))
+    neg = math.copysign(1.0, v) < 0
+    fin = [c for c in range(256) if np.isfinite(t[c]) and bool(c & 0x80) == neg]
+    if abs(v) >= FMAX[fmt]:
+        return next(c for c in fin if abs(t[c]) == FMAX[fmt])
+    best = min(abs(t[c] - v) for c in fin)
+    cands = [c for c in fin if abs(t[c] - v) == best]
+    if len(cands) == 1:
+        return cands[0]
+    return next(c for c in cands if c % 2 == 0)
+
+
+@pytest.mark.parametrize("fmt", [oracle.E4M3, oracle.E5M2])
+def test_encode_equals_brute_force_at_midpoints(fmt):
+    """Every midpoint between neighbouring finite values, one float32 step on
+    either side of it, and every code's own value."""
+    t = oracle.decode_table(fmt)
+    pos = sorted({t[c] for c in range(128) if np.isfinite(t[c])})
+    vals = []
+    for a, b in zip(pos[:-1], pos[1:]):
+        mid = np.float32((a + b) / 2)
+        assert float(mid) == (a + b) / 2  # midpoints are exact in float32
+        vals += [mid, np.nextafter(mid, np.float32(0)), np.nextafter(mid, np.float32(np.inf))]
+    vals += [np.float32(p) for p in pos]
+    vals = vals + [-v for v in vals]
+    for v in vals:
+        assert oracle.encode_fp8(fmt, v) == _encode_brute(fmt, v), (fmt, float(v))
+
+
+@pytest.mark.parametrize("fmt,tdt", [(oracle.E4M3, torch.float8_e4m3fn), (oracle.E5M2, torch.float8_e5m2)])
+def test_encode_matches_torch_float8_in_range(fmt, tdt):
+    """Quantizing a group whose largest magnitude is exactly fmax gives scale 1,
+    so its codes are the encoder's codes of the values themselves; torch's
+    float8 conversion (nearest even) must agree on 30k log-uniform values
+    spanning the subnormals up to fmax."""
+    rng = wl.rng_for(4242 + fmt)
+    fmax = FMAX[fmt]
+    lo = math.log2(fmax) - (26 if fmt == oracle.E4M3 else 40)
+    mag = np.exp2(rng.uniform(lo, math.log2(fmax), size=(240, 127)))
+    x = (mag * rng.choice([-1.0, 1.0], size=mag.shape)).astype(np.float32)
+    x = np.concatenate([np.full((240, 1), fmax, np.float32), x], axis=1)  # amax = fmax
+    q, s = oracle.quantize_per_token(x, fmt)
+    assert np.all(s == 1.0)
+    ref = torch.from_numpy(x).to(tdt).view(torch.uint8).numpy()
+    assert np.array_equal(q, ref)
+
+
+@pytest.mark.parametrize("fmt", [oracle.E4M3, oracle.E5M2])
+@pytest.mark.parametrize("k", [16, 128, 300, 7168])
+def test_quantize_matches_generator(fmt, k):
+    """The generator's quantizer (numpy float32 division, torch float8) is an
+    independent statement of the same steps."""
+    rng = wl.rng_for(77 + k + fmt)
+    x = rng.standard_normal((3, 45, k)).astype(np.float32)
+    x *= np.exp2(rng.integers(-20, 20, size=(3, 45, 1))).astype(np.float32)  # per-row magnitudes
+    x[0, 5, :] = 0.0                       # an all-zero row (all its groups zero)
+    x[1, 7, : min(k, 128)] = 0.0           # one zero group
+    x[2, 3, 0] = 3.0e38                    # a huge value (scale stays finite)
+    q, s = oracle.quantize_per_token(x, fmt)
+    q2, s2 = wl.quantize_rows(x, fmt)
+    assert np.array_equal(s, s2)
+    assert np.array_equal(q, q2)
+
+
+def test_quantize_brute_force_tiny():
+    """Two rows of 144 columns (a full group and a 16-wide tail), every step
+    written out with Python floats rounded to float32 and the brute-force
+    encoder."""
+    rng = wl.rng_for(5)
+    x = (rng.standard_normal((2, 144)) * 3).astype(np.float32)
+    for fmt in (oracle.E4M3, oracle.E5M2):
+        q, s = oracle.quantize_per_token(x, fmt)
+        for r in range(2):
+            for g, (c0, c1) in enumerate([(0, 128), (128, 144)]):
+                amax = max(abs(float(v)) for v in x[r, c0:c1])
+                sc = np.float32(np.float32(amax) / np.float32(FMAX[fmt]))
+                assert s[r, g] == sc
+                for c in range(c0, c1):
+                    assert q[r, c] == _encode_brute(fmt, np.float32(x[r, c]) / sc)
+
+
+@pytest.mark.parametrize("fmt", [oracle.E4M3, oracle.E5M2])
+def test_quantize_closed_forms(fmt):
+    """Each nonzero group reaches +-fmax at its largest element, its scale is
+    amax / fmax, the dequantized values are within half an FP8 step of the
+    inputs, and a zero group gets scale 1 with zero codes."""
+    rng = wl.rng_for(99 + fmt)
+    x = rng.standard_normal((64, 384)).astype(np.float32)
+    x[10, 128:256] = 0.0
+    q, s = oracle.quantize_per_token(x, fmt)
+    t = oracle.decode_table(fmt)
+    dq = t[q]
+    mbits = 3 if fmt == oracle.E4M3 else 2
+    min_normal = 2.0 ** -6 if fmt == oracle.E4M3 else 2.0 ** -14
+    for r in range(64):
+        for g in range(3):
+            xs = x[r, 128 * g:128 * (g + 1)].astype(np.float64)
+            d = dq[r, 128 * g:128 * (g + 1)]
+            if not np.any(xs):
+                assert s[r, g] == 1.0 and np.all(q[r, 128 * g:128 * (g + 1)] == 0)
+                continue
+            amax = np.abs(xs).max()
+            assert s[r, g] == np.float32(np.float32(amax) / np.float32(FMAX[fmt]))
+            assert np.abs(d).max() == FMAX[fmt]
+            v = xs / float(s[r, g])
+            step = np.where(np.abs(v) >= min_normal,
+                            np.exp2(np.floor(np.log2(np.maximum(np.abs(v), min_normal))) - mbits),
+                            min_normal * 2.0 ** -mbits)
+            # half a step, plus the float32 rounding of the division
+            assert np.all(np.abs(d - v) <= step / 2 + np.abs(v) * 2.0 ** -23)
+            assert np.all((np.sign(d) == np.sign(v)) | (d == 0))
