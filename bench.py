@@ -223,6 +223,58 @@ def oracle_sample_rate(probs, shapes, seconds: float, seed: int = 0):
 
 # ------------------------------------------------------------------ arms
 
+def quantize_bytes(rows, k):
+    """Algorithmic HBM bytes of one per-token quantization: BF16 X read once,
+    FP8 A and one FP32 scale per row and 128-wide K block written once."""
+    return rows * k * 2 + rows * k + rows * ((k + 127) // 128) * 4
+
+
+def measure_quantize(fg, torch, dev, stream, hbm_peak, peak_src, reps=20):
+    """Per-token FP8 quantization of the sweep's m = 4096 activations
+    (BF16 [4096][k], k in the sweep), each shape rotating over copies of X, A
+    and sA larger than twice L2; `reps` back-to-back launches between CUDA
+    events on the launching stream, after a warm-up."""
+    ks = sorted({k for (_, k) in wl.DENSE_SWEEP_NK})
+    rows_out, tot_b, tot_s = [], 0.0, 0.0
+    for k in ks:
+        m = max(wl.DENSE_SWEEP_M)
+        x = torch.from_numpy(wl.activations((m, k), seed=wl.seed_for(1, 50 + k % 97))).to(torch.bfloat16).to(dev)
+        nb = quantize_bytes(m, k)
+        ncopy = max(2, -(-ROTATE_BYTES // nb))
+        copies = [(x.clone(), torch.empty((m, k), dtype=torch.float8_e4m3fn, device=dev),
+                   torch.empty(((k + 127) // 128, fg.fg_scales_a_ld(m)), dtype=torch.float32, device=dev))
+                  for _ in range(ncopy)]
+        del x
+        for X, A, sA in copies[:3]:
+            fg.fg_quantize_fp8_per_token(X, A, sA, stream=stream)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for r in range(reps):
+            X, A, sA = copies[r % ncopy]
+            fg.fg_quantize_fp8_per_token(X, A, sA, stream=stream)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        us = e0.elapsed_time(e1) * 1e3 / reps
+        rows_out.append({"m": m, "k": k, "us": round(us, 2), "gbs": round(nb / (us * 1e-6) / 1e9, 1),
+                         "algorithmic_bytes": nb})
+        tot_b += nb
+        tot_s += us * 1e-6
+        del copies
+    st, _ = fg.fg_get_device_status()
+    if st != 0:
+        raise RuntimeError(f"device status {st} after the quantization runs")
+    ach = tot_b / tot_s / 1e9
+    return {"kernel": "fg::quantize_per_token_kernel<E4M3>",
+            "workload": "BF16 activations [4096][k] -> FP8 E4M3 A + MN-major 1x128 FP32 scales, k in the sweep",
+            "roofline": {"bound": "hbm", "achieved": round(ach, 1), "peak": hbm_peak, "unit": "GB/s",
+                         "frac": round(ach / hbm_peak, 3), "traffic": None,
+                         "peak_source": f"{peak_src}: hbm copy"},
+            "timing": (f"{reps} back-to-back launches per shape between CUDA events, rotating over copies "
+                       ">= 272 MiB (> 2 x L2), after the GEMM steps"),
+            "shapes": rows_out}
+
+
 def run_reference(args, ws, rank):
     if rank != 0:
         return
@@ -419,6 +471,10 @@ def run_ours(args, ws, rank, local):
                         "timing": "per-problem back-to-back launches after the timed steps",
                         "peak_source": f"{peak_src}: hbm copy"}
 
+    quant = None
+    if not args.no_quantize:
+        quant = measure_quantize(fg, torch, dev, stream, hbm_peak, peak_src)
+
     # ------------------------------------------------ end to end (host buffers)
     e2e = None
     if not args.no_e2e:
@@ -523,6 +579,7 @@ def run_ours(args, ws, rank, local):
             "roofline": roofline, "roofline_other_kernels": others, "roofline_hbm": roofline_hbm,
             "shapes": shape_rows, "clocks": clock_info, "e2e": e2e,
             "gpu_launches": len(items) * args.steps, "cpu_baseline": cpu,
+            "quantize_per_token": quant,
         }
         print(json.dumps(line), flush=True)
 
@@ -536,6 +593,7 @@ def main(argv=None):
     ap.add_argument("--shapes", default="", help="restrict to 'm,n,k;m,n,k' (profiling)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-quantize", action="store_true", help="skip the activation-quantization figures")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     args = ap.parse_args(argv)
     if args.warmup < 3 and args.impl == "ours" and not args.shapes:

@@ -103,6 +103,34 @@ fg_status fg_grouped_gemm_fp8_masked(const void *A, int a_fmt, const float *sA, 
 fg_status fg_scales_a_to_mn_major(const float *src, float *dst, int batches, int rows, int kb,
                                   int ld_dst, void *stream);
 
+/* Per-token FP8 quantization of activations: the step that produces a GEMM
+ * call's LHS (page "DeepSeek开源周第三天DeepGEMM", section "基本用法": FP8 LHS
+ * with one FP32 scale per row and 128-wide K block, scales in the MN-major
+ * layout; page "企业官网建设流程全解析", section 5.2: each scale comes from a
+ * scan of its group for the largest magnitude).  For row r of batch b and K
+ * block kb, over the block's columns inside k:
+ *
+ *   amax = max |X|,  sA = amax / fmax (1 when amax == 0),  A = fp8(X / sA)
+ *
+ * with fmax 448 (E4M3) or 57344 (E5M2), float32 IEEE divisions and round to
+ * nearest even, saturating at +-fmax.
+ *   X   [batches][rows][ld_x] bfloat16 (device), 16-byte aligned, ld_x >= k,
+ *       ld_x % 8 == 0; finite values (codes for Inf/NaN inputs are unspecified)
+ *   A   [batches][rows][k] FP8 bytes (device), 16-byte aligned, k % 16 == 0
+ *   sA  [batches][ceil(k/128)][ld_sA] floats (device), 16-byte aligned,
+ *       ld_sA >= rows, ld_sA % 4 == 0: the layout every GEMM call above takes
+ *       (dense and contiguous: batches = 1; masked: batches = G, rows = M_cap)
+ *   masked_m  NULL (all rows), or [batches] int32 counts on the device: rows
+ *       r >= masked_m[b] of A and sA are left untouched; a count outside
+ *       [0, rows] is clamped into it and recorded as FG_ERR_DEVICE_CHECK
+ *       (detail: the batch index).
+ * Entries of sA past `rows` are not written.  rows == 0 is a no-op.
+ * Asynchronous on `stream`, no allocation, CUDA-graph capturable; launched
+ * with programmatic dependent launch when that is on (it then waits for the
+ * previous kernel of the stream before its first read). */
+fg_status fg_quantize_fp8_per_token(const void *X, int ld_x, int fmt, void *A, float *sA, int ld_sA,
+                                    const int32_t *masked_m, int batches, int rows, int k, void *stream);
+
 /* Smallest valid ld_sA for `rows` rows: rows rounded up to a multiple of 4. */
 int fg_scales_a_ld(int rows);
 

@@ -42,6 +42,7 @@ SIGNATURES = {
     "fg_grouped_gemm_fp8_masked": (_I, [_P, _I, _P, _I, _P, _I, _P, _P, _P, _I, _I, _I, _I, _P]),
     "fg_scales_a_to_mn_major": (_I, [_P, _P, _I, _I, _I, _I, _P]),
     "fg_scales_a_ld": (_I, [_I]),
+    "fg_quantize_fp8_per_token": (_I, [_P, _I, _I, _P, _P, _I, _P, _I, _I, _I, _P]),
     "fg_get_device_status": (_I, [_P, ctypes.POINTER(_U32)]),
     "fg_set_num_sms": (_I, [_I]),
     "fg_set_watchdog_ms": (_I, [_U32]),
@@ -201,6 +202,54 @@ def fg_scales_a_to_mn_major(src, dst=None, *, stream=None):
                                         _stream_ptr(stream))
     _check("fg_scales_a_to_mn_major", st)
     return dst
+
+
+def fg_quantize_fp8_per_token(X, A=None, sA=None, *, fmt=E4M3, masked_m=None, stream=None):
+    """Per-token (1x128) FP8 quantization of BF16 activations X [rows, k] or
+    [batches, rows, k] into A (same shape, FP8) and MN-major sA [.., kb, ld].
+
+    X may be a column slice of a wider matrix (last stride 1, rows ld_x apart,
+    batches rows * ld_x apart).  A and sA are allocated when not given (sA with
+    ld = fg_scales_a_ld(rows); its padding entries are left unwritten).  With
+    masked_m ([batches] int32 on the device) rows r >= masked_m[b] are left
+    untouched.  Returns (A, sA)."""
+    if not isinstance(X, torch.Tensor) or not X.is_cuda or X.dtype != torch.bfloat16:
+        raise TypeError("X must be a CUDA bfloat16 tensor")
+    if X.dim() not in (2, 3):
+        raise ValueError("X must be [rows, k] or [batches, rows, k]")
+    batches = 1 if X.dim() == 2 else X.shape[0]
+    rows, k = X.shape[-2], X.shape[-1]
+    if rows > 1:
+        ld_x = X.stride(-2)
+    else:  # one row per batch: the batch stride is the row pitch
+        ld_x = X.stride(0) if X.dim() == 3 and batches > 1 else k
+    if X.stride(-1) != 1 or (X.dim() == 3 and batches > 1 and X.stride(0) != rows * ld_x):
+        raise ValueError("X must have unit column stride and batches rows * ld_x apart")
+    lead = () if X.dim() == 2 else (batches,)
+    kb = _cdiv(k, 128)
+    fdt = torch.float8_e4m3fn if int(fmt) == E4M3 else torch.float8_e5m2
+    if A is None:
+        A = torch.empty(lead + (rows, k), dtype=fdt, device=X.device)
+    else:
+        _need(A, "A", _FP8, X.dim())
+        if tuple(A.shape) != lead + (rows, k):
+            raise ValueError("A shape does not fit X")
+    if sA is None:
+        sA = torch.empty(lead + (kb, fg_scales_a_ld(rows)), dtype=torch.float32, device=X.device)
+    else:
+        _need(sA, "sA", _F32, X.dim())
+        if tuple(sA.shape[:-1]) != lead + (kb,) or sA.shape[-1] < rows:
+            raise ValueError("sA shape does not fit X")
+    mp = 0
+    if masked_m is not None:
+        _need(masked_m, "masked_m", _I32, 1)
+        if masked_m.shape[0] != batches:
+            raise ValueError("masked_m must hold one count per batch")
+        mp = masked_m.data_ptr()
+    st = lib().fg_quantize_fp8_per_token(X.data_ptr(), ld_x, int(fmt), A.data_ptr(), sA.data_ptr(),
+                                         sA.shape[-1], mp, batches, rows, k, _stream_ptr(stream))
+    _check("fg_quantize_fp8_per_token", st)
+    return A, sA
 
 
 def fg_get_device_status(stream=None):

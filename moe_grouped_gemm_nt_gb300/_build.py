@@ -15,7 +15,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(BUILD_DIR, "libfp8gemm.so")
 SOURCES = ["fp8gemm.cu"]
-HEADERS = ["gemm_kernel.cuh", "ptx.cuh"]
+HEADERS = ["gemm_kernel.cuh", "gemm_pair_kernel.cuh", "quantize_kernel.cuh", "ptx.cuh"]
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -14,6 +14,7 @@
 #include "../../include/fp8gemm.h"
 #include "gemm_kernel.cuh"
 #include "gemm_pair_kernel.cuh"
+#include "quantize_kernel.cuh"
 
 namespace {
 
@@ -433,6 +434,49 @@ fg_status fg_scales_a_to_mn_major(const float *src, float *dst, int batches, int
     dim3 grid((unsigned)cdiv(ld_dst, 256), (unsigned)kb, (unsigned)batches);
     fg::scales_to_mn_major_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(src, dst, rows, kb, ld_dst);
     return cudaPeekAtLastError() == cudaSuccess ? FG_OK : FG_ERR_CUDA;
+}
+
+fg_status fg_quantize_fp8_per_token(const void *X, int ld_x, int fmt, void *A, float *sA, int ld_sA,
+                                    const int32_t *masked_m, int batches, int rows, int k, void *stream) {
+    if (!X || !A || !sA || batches < 1 || rows < 0 || k < 1 || ld_x < k || ld_sA < rows || ld_sA < 1)
+        return FG_ERR_INVALID_ARG;
+    if (fmt != FG_E4M3 && fmt != FG_E5M2) return FG_ERR_INVALID_ARG;
+    if (!aligned16(X) || !aligned16(A) || !aligned16(sA) || ld_x % 8 != 0 || ld_sA % 4 != 0)
+        return FG_ERR_MISALIGNED;
+    if (k % 16 != 0) return FG_ERR_UNSUPPORTED;
+    const int kb = cdiv(k, 128);
+    if (kb > 65535 || batches > 65535) return FG_ERR_UNSUPPORTED;
+    if (rows == 0) return FG_OK;
+    DeviceInfo *dev = nullptr;
+    if (fg_status st = device_info(&dev); st != FG_OK) return st;
+
+    fg::QuantParams p{};
+    p.x = static_cast<const uint16_t *>(X);
+    p.a = static_cast<uint8_t *>(A);
+    p.sa = sA;
+    p.masked_m = masked_m;
+    p.status = dev->status;
+    p.ld_x = ld_x;
+    p.ld_sa = ld_sA;
+    p.rows = rows;
+    p.k = k;
+    p.kb = kb;
+
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3((unsigned)cdiv(rows, fg::QUANT_ROWS), (unsigned)kb, (unsigned)batches);
+    cfg.blockDim = dim3(fg::QUANT_THREADS, 1, 1);
+    cfg.stream = static_cast<cudaStream_t>(stream);
+    cudaLaunchAttribute at[1];
+    if (g_pdl.load() != 0) {
+        at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        at[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = at;
+        cfg.numAttrs = 1;
+    }
+    const cudaError_t e = fmt == FG_E4M3 ? cudaLaunchKernelEx(&cfg, fg::quantize_per_token_kernel<0>, p)
+                                         : cudaLaunchKernelEx(&cfg, fg::quantize_per_token_kernel<1>, p);
+    if (e != cudaSuccess) return cuda_fail();
+    return cudaPeekAtLastError() == cudaSuccess ? FG_OK : cuda_fail();
 }
 
 int fg_scales_a_ld(int rows) { return rows <= 0 ? 4 : (rows + 3) / 4 * 4; }

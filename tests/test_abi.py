@@ -92,3 +92,30 @@ def test_tuning_knob_argument_checks():
     out = ctypes.c_int(0)
     assert h.fg_query_dense_plan_ex(128, 256, 512, ctypes.byref(out), ctypes.byref(out), None) == 1
     assert h.fg_query_dense_plan(0, 256, 512, ctypes.byref(out), ctypes.byref(out)) == 1
+
+
+def test_quantize_argument_checks():
+    """fg_quantize_fp8_per_token rejects bad arguments on the host, before any
+    CUDA call (the pointers here are never dereferenced)."""
+    Q = fg.lib().fg_quantize_fp8_per_token
+    #        X     ld_x fmt A     sA    ld_sA masked batches rows k
+    ok = [FAKE, 256, 0, FAKE, FAKE, 64, None, 1, 64, 256, None]
+
+    def call(**kw):
+        names = ["X", "ld_x", "fmt", "A", "sA", "ld_sA", "masked", "batches", "rows", "k", "stream"]
+        args = dict(zip(names, ok))
+        args.update(kw)
+        return Q(*[args[n] for n in names])
+
+    assert call(X=None) == 1 and call(A=None) == 1 and call(sA=None) == 1
+    assert call(fmt=2) == 1 and call(fmt=-1) == 1
+    assert call(ld_x=128) == 1            # ld_x < k
+    assert call(ld_sA=60) == 1            # ld_sA < rows
+    assert call(batches=0) == 1 and call(rows=-1) == 1 and call(k=0) == 1
+    assert call(X=FAKE + 4) == 2 and call(A=FAKE + 8) == 2 and call(sA=FAKE + 4) == 2
+    assert call(ld_x=260) == 2            # rows of X must stay 16-byte aligned
+    assert call(ld_sA=66) == 2            # the GEMM's sA rule: ld_sA % 4 == 0
+    assert call(k=136, ld_x=136) == 3     # k % 16 != 0
+    assert call(k=128 * 65536, ld_x=128 * 65536) == 3  # more K blocks than a grid dimension holds
+    assert call(batches=65536) == 3
+    assert call(rows=0) == 0              # nothing to do: no launch

@@ -317,3 +317,37 @@ def large_dense_shapes():
     """(m, n, k, b_fmt) of workload 4: 8192^3, the K-tail case, the E5M2-B case."""
     return [(8192, 8192, 8192, E4M3), (8192, 8192, 8192 + 128 * 3, E4M3),
             (8192, 8192, 8192, E5M2)]
+
+
+def activations(shape, seed: int, outlier_frac: float = 0.01, outlier_gain: float = 32.0,
+                chunk_rows: int = 4096) -> np.ndarray:
+    """Seeded BF16 activations [..., rows, k], returned as float32 numpy values
+    that are exactly bfloat16 (rounded to nearest even by torch).
+
+    Recipe: N(0,1) entries; each row scaled by 2^u with u uniform in [-6, 6]
+    (tokens of different magnitude); a fixed random ~1% of the columns (outlier
+    channels) multiplied by `outlier_gain`.  Drawn in row chunks to bound peak
+    memory."""
+    import torch
+
+    shape = tuple(shape)
+    rng = rng_for(seed)
+    k = shape[-1]
+    out = _normal(rng, shape, chunk_rows)
+    flat = out.reshape(-1, k)
+    rows_total = flat.shape[0]
+    gain = np.exp2(rng.uniform(-6.0, 6.0, size=(rows_total, 1))).astype(np.float32)
+    cols = np.ones(k, np.float32)
+    cols[rng.random(k) < outlier_frac] = np.float32(outlier_gain)
+    for r0 in range(0, rows_total, chunk_rows):
+        r1 = min(r0 + chunk_rows, rows_total)
+        blk = flat[r0:r1] * gain[r0:r1] * cols
+        flat[r0:r1] = torch.from_numpy(blk).to(torch.bfloat16).to(torch.float32).numpy()
+    return out
+
+
+def bf16_bits(x: np.ndarray) -> np.ndarray:
+    """Bit patterns (uint16) of float32 values that are exactly bfloat16."""
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    assert not np.any(u & 0xFFFF), "values are not bfloat16"
+    return (u >> 16).astype(np.uint16)
