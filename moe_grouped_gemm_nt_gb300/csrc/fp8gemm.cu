@@ -404,6 +404,30 @@ fg_status run(const void *A, int a_fmt, const float *sA, int ld_sA, const void *
 
 }  // namespace
 
+namespace {
+// Dynamic shared memory attribute of the quantization kernel and its resident
+// CTAs per SM (occupancy query), once per device and format; 0 on failure.
+int quantize_blocks_per_sm(int fmt) {
+    static std::atomic<int> cache[kMaxDevices][2];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+    const int v = cache[dev][fmt].load();
+    if (v > 0) return v;
+    auto kernel = fmt == FG_E4M3 ? fg::quantize_per_token_kernel<0> : fg::quantize_per_token_kernel<1>;
+    int n = 0;
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, fg::QUANT_SMEM_BYTES) !=
+            cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, fg::QUANT_THREADS, fg::QUANT_SMEM_BYTES) !=
+            cudaSuccess ||
+        n <= 0) {
+        cudaGetLastError();
+        return 0;
+    }
+    cache[dev][fmt].store(n);
+    return n;
+}
+}  // namespace
+
 extern "C" {
 
 fg_status fg_gemm_fp8_nt(const void *A, int a_fmt, const float *sA, int ld_sA, const void *B, int b_fmt,
@@ -447,8 +471,15 @@ fg_status fg_quantize_fp8_per_token(const void *X, int ld_x, int fmt, void *A, f
     const int kb = cdiv(k, 128);
     if (kb > 65535 || batches > 65535) return FG_ERR_UNSUPPORTED;
     if (rows == 0) return FG_OK;
+    const long long units = (long long)batches * cdiv(rows, fg::QUANT_ROWS) * kb;
+    if (units > 0x7FFFFFFFLL - (1LL << 20)) return FG_ERR_UNSUPPORTED;  // unit index + grid stays in int
     DeviceInfo *dev = nullptr;
     if (fg_status st = device_info(&dev); st != FG_OK) return st;
+    const int per_sm = quantize_blocks_per_sm(fmt);
+    if (per_sm <= 0) return cuda_fail();
+    int sms = dev->num_sms;
+    const int ovr = g_num_sms_override.load();
+    if (ovr > 0 && ovr < sms) sms = ovr;
 
     fg::QuantParams p{};
     p.x = static_cast<const uint16_t *>(X);
@@ -461,10 +492,16 @@ fg_status fg_quantize_fp8_per_token(const void *X, int ld_x, int fmt, void *A, f
     p.rows = rows;
     p.k = k;
     p.kb = kb;
+    p.timeout_ns = (unsigned long long)g_watchdog_ms.load() * 1000000ull;
+    p.debug_skip_unit = g_debug_skip_iter.exchange(-1);
+    p.row_blocks = cdiv(rows, fg::QUANT_ROWS);
+    p.units = (int)units;
 
+    // persistent CTAs: as many as are resident at once, each walks the units
     cudaLaunchConfig_t cfg{};
-    cfg.gridDim = dim3((unsigned)cdiv(rows, fg::QUANT_ROWS), (unsigned)kb, (unsigned)batches);
+    cfg.gridDim = dim3((unsigned)std::min<long long>(units, (long long)sms * per_sm), 1, 1);
     cfg.blockDim = dim3(fg::QUANT_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = fg::QUANT_SMEM_BYTES;
     cfg.stream = static_cast<cudaStream_t>(stream);
     cudaLaunchAttribute at[1];
     if (g_pdl.load() != 0) {
@@ -473,8 +510,17 @@ fg_status fg_quantize_fp8_per_token(const void *X, int ld_x, int fmt, void *A, f
         cfg.attrs = at;
         cfg.numAttrs = 1;
     }
-    const cudaError_t e = fmt == FG_E4M3 ? cudaLaunchKernelEx(&cfg, fg::quantize_per_token_kernel<0>, p)
-                                         : cudaLaunchKernelEx(&cfg, fg::quantize_per_token_kernel<1>, p);
+    // X as a 3-D tensor {k, rows, batches}; one box = one unit (128 columns x 64 rows)
+    CUtensorMap tx;
+    {
+        const uint64_t dims[3] = {(uint64_t)k, (uint64_t)rows, (uint64_t)batches};
+        const uint64_t strides[2] = {(uint64_t)ld_x * 2, (uint64_t)ld_x * 2 * (uint64_t)rows};
+        const uint32_t box[3] = {128, (uint32_t)fg::QUANT_ROWS, 1};
+        if (!encode(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, X, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE))
+            return cuda_fail();
+    }
+    const cudaError_t e = fmt == FG_E4M3 ? cudaLaunchKernelEx(&cfg, fg::quantize_per_token_kernel<0>, tx, p)
+                                         : cudaLaunchKernelEx(&cfg, fg::quantize_per_token_kernel<1>, tx, p);
     if (e != cudaSuccess) return cuda_fail();
     return cudaPeekAtLastError() == cudaSuccess ? FG_OK : cuda_fail();
 }
@@ -549,7 +595,9 @@ fg_status fg_set_watchdog_ms(uint32_t ms) {
 
 // Test hook (not part of the public header): in the next GEMM call, the
 // producer of every CTA leaves its K iteration `iter` unarmed, so the MMA
-// warp's bounded wait expires and the call reports FG_ERR_TIMEOUT.
+// warp's bounded wait expires and the call reports FG_ERR_TIMEOUT; in the next
+// quantization call, every CTA's producer leaves its unit number `iter`
+// unfilled, with the same outcome for the consumer warps.
 fg_status fg_debug_skip_producer_iteration(int iter) {
     g_debug_skip_iter.store(iter);
     return FG_OK;

@@ -111,6 +111,35 @@ def test_quantize_special_values(fmt):
     _check_against_oracle(x, fmt, A, sA)
 
 
+@pytest.mark.parametrize("fmt", [wl.E4M3, wl.E5M2])
+def test_quantize_extreme_dynamic_range(fmt):
+    """Magnitudes log-uniform over the whole BF16 range (2^-133 .. 2^127) with
+    per-group ceilings, so groups have scales from float32 subnormals to 2^119
+    and elements from far below to exactly at the group maximum: the
+    quotient's rounding (including ties of the FP8 rounding and zeros of
+    either sign) must match an IEEE division everywhere."""
+    rng = wl.rng_for(2024 + fmt)
+    rows, k = 96, 1024
+    ceil = rng.uniform(-133, 127, size=(rows, k // 128, 1))
+    e = ceil - rng.uniform(0, 60, size=(rows, k // 128, 128))
+    x = np.exp2(np.maximum(e, -133)) * rng.choice([-1.0, 1.0], size=e.shape)
+    x = x.reshape(rows, k).astype(np.float32)
+    x = torch.from_numpy(x).to(torch.bfloat16).to(torch.float32).numpy()
+    A, sA = _run(x, fmt)
+    _check_against_oracle(x, fmt, A, sA)
+
+
+def test_quantize_walks_many_units_per_cta():
+    """With the SM limit at 1 each persistent CTA walks hundreds of units."""
+    x = wl.activations((2, 300, 2048), seed=16)
+    fg.fg_set_num_sms(1)
+    try:
+        A, sA = _run(x, wl.E5M2, masked_m=[300, 123])
+    finally:
+        fg.fg_set_num_sms(0)
+    _check_against_oracle(x, wl.E5M2, A, sA, limits=[300, 123])
+
+
 def test_quantize_masked_counts():
     """Rows past each batch's device-side count stay untouched."""
     x = wl.activations((4, 96, 512), seed=8)

@@ -60,3 +60,30 @@ def test_unarmed_stage_times_out_and_context_survives(short_watchdog, skip_iter)
 def test_status_is_cleared_by_reading():
     st, _ = fg.fg_get_device_status()
     assert st == fg.FG_OK
+
+
+@pytest.mark.parametrize("skip_unit", [0, 5])
+def test_quantizer_unfilled_stage_times_out_and_context_survives(skip_unit):
+    """The quantizer's producer leaves one unit unfilled in every CTA: the
+    consumers' bounded wait expires, the CTA drains the copies it issued and
+    returns, and the next call is bit-exact."""
+    x = wl.activations((4096, 1024), seed=91)  # 1024 units of 32 rows x 128 columns
+    X = torch.from_numpy(x).to(torch.bfloat16).cuda()
+    fg.fg_set_watchdog_ms(200)
+    fg.fg_set_num_sms(4)  # a few persistent CTAs, each with many units
+    try:
+        assert fg.fg_get_device_status()[0] == fg.FG_OK
+        fg.lib().fg_debug_skip_producer_iteration(skip_unit)
+        fg.fg_quantize_fp8_per_token(X)
+        st, detail = fg.fg_get_device_status()
+        assert st == 5, fg.STATUS_NAMES.get(st, st)  # FG_ERR_TIMEOUT
+        assert (detail >> 24) in (1, 3)              # producer or consumer wait
+    finally:
+        fg.fg_set_watchdog_ms(0)
+        fg.fg_set_num_sms(0)
+        fg.lib().fg_debug_skip_producer_iteration(-1)
+    A, sA = fg.fg_quantize_fp8_per_token(X)
+    q, s = oracle.quantize_per_token(x, wl.E4M3)
+    assert np.array_equal(A.view(torch.uint8).cpu().numpy(), q)
+    assert np.array_equal(sA[:, :4096].cpu().numpy(), s.T)
+    assert fg.fg_get_device_status()[0] == fg.FG_OK
