@@ -94,7 +94,8 @@ def kernel_sources_digest():
 
 def load_traffic():
     """{(m, n, k): DRAM bytes per launch} from profiles/dram_traffic.txt lines
-    '<digest> <m> <n> <k> <read+write bytes>' of the current sources."""
+    '<digest> <m> <n> <k> <read+write bytes>' of the current sources (n = 0:
+    the activation quantizer on [m][k])."""
     out = {}
     path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
     if not os.path.exists(path):
@@ -229,7 +230,7 @@ def quantize_bytes(rows, k):
     return rows * k * 2 + rows * k + rows * ((k + 127) // 128) * 4
 
 
-def measure_quantize(fg, torch, dev, stream, hbm_peak, peak_src, reps=20):
+def measure_quantize(fg, torch, dev, stream, hbm_peak, peak_src, reps=20, traffic_tab=None):
     """Per-token FP8 quantization of the sweep's m = 4096 activations
     (BF16 [4096][k], k in the sweep), each shape rotating over copies of X, A
     and sA larger than twice L2; `reps` back-to-back launches between CUDA
@@ -257,7 +258,7 @@ def measure_quantize(fg, torch, dev, stream, hbm_peak, peak_src, reps=20):
         torch.cuda.synchronize()
         us = e0.elapsed_time(e1) * 1e3 / reps
         rows_out.append({"m": m, "k": k, "us": round(us, 2), "gbs": round(nb / (us * 1e-6) / 1e9, 1),
-                         "algorithmic_bytes": nb})
+                         "algorithmic_bytes": nb, "traffic": (traffic_tab or {}).get((m, 0, k))})
         tot_b += nb
         tot_s += us * 1e-6
         del copies
@@ -265,10 +266,13 @@ def measure_quantize(fg, torch, dev, stream, hbm_peak, peak_src, reps=20):
     if st != 0:
         raise RuntimeError(f"device status {st} after the quantization runs")
     ach = tot_b / tot_s / 1e9
+    known = [r["traffic"] for r in rows_out]
+    traffic = sum(known) / len(known) if all(v is not None for v in known) else None
     return {"kernel": "fg::quantize_per_token_kernel<E4M3>",
+            "algorithmic_bytes_per_launch": tot_b / len(rows_out),
             "workload": "BF16 activations [4096][k] -> FP8 E4M3 A + MN-major 1x128 FP32 scales, k in the sweep",
             "roofline": {"bound": "hbm", "achieved": round(ach, 1), "peak": hbm_peak, "unit": "GB/s",
-                         "frac": round(ach / hbm_peak, 3), "traffic": None,
+                         "frac": round(ach / hbm_peak, 3), "traffic": traffic,
                          "peak_source": f"{peak_src}: hbm copy"},
             "timing": (f"{reps} back-to-back launches per shape between CUDA events, rotating over copies "
                        ">= 272 MiB (> 2 x L2), after the GEMM steps"),
@@ -473,7 +477,7 @@ def run_ours(args, ws, rank, local):
 
     quant = None
     if not args.no_quantize:
-        quant = measure_quantize(fg, torch, dev, stream, hbm_peak, peak_src)
+        quant = measure_quantize(fg, torch, dev, stream, hbm_peak, peak_src, traffic_tab=traffic_tab)
 
     # ------------------------------------------------ end to end (host buffers)
     e2e = None

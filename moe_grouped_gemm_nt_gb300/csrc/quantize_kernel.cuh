@@ -14,18 +14,20 @@
 // quotients, and round-to-nearest-even, saturating conversion to FP8.
 //
 // The work is bound by HBM bandwidth: 2 bytes read and 1 + 4/128 bytes written
-// per element.  A unit of work is 64 rows x one 128-column K block (16 KB of
-// X).  CTAs are persistent (as many as fit on the SMs); each takes a
-// contiguous range of units, walked along K.  One producer thread loads each
-// unit with a single 3-D TMA box (columns past k and rows past the batch read
-// as zeros) into a ring of QUANT_STAGES shared-memory stages, so several units
-// per CTA are in flight while eight consumer warps work.  Each row is handled
-// by 4 consecutive lanes with 32 columns each (four 16-byte chunks; odd rows
-// take the chunks in the other order, so every quarter-warp's shared loads
-// hit 32 distinct banks); the group maximum runs on BF16 pairs
-// (max.xorsign.abs: the larger magnitude of each half) and needs two
-// butterfly shuffles.  A consumer warp releases its stage as soon as the
-// values are in registers, then writes its codes (8-byte stores, 32
+// per element.  A unit of work is 32 rows x one 128-column K block (8 KB of
+// X).  CTAs are persistent (as many as fit on the SMs: seven per SM, by registers);
+// each takes a contiguous range of units, walked along K.  One producer
+// thread loads each unit with a single 3-D TMA box (columns past k and rows
+// past the batch read as zeros) into the CTA's shared-memory stage; four
+// consumer warps copy it to registers and release it at once, so the next
+// unit's load overlaps their arithmetic and stores.  (Rings of two to four
+// stages per CTA, and 64-row units with eight consumer warps, measured
+// slower: more small CTAs per SM keep HBM busier than deeper rings.)  Each
+// row is handled by 4 consecutive lanes with 32 columns each (four 16-byte
+// chunks; odd rows take the chunks in the other order, so every quarter-
+// warp's shared loads hit 32 distinct banks); the group maximum runs on BF16
+// pairs (max.xorsign.abs: the larger magnitude of each half) and needs two
+// butterfly shuffles.  A consumer warp writes its codes (8-byte stores, 32
 // contiguous bytes per row and store) and the row's scale (8 rows of a warp:
 // 32 contiguous bytes of sA).  Every wait is bounded by a %globaltimer
 // watchdog: on expiry the CTA records FG_ERR_TIMEOUT, stops, and waits (again
@@ -77,11 +79,11 @@ struct QuantParams {
     int debug_skip_unit;       // producers leave their unit with this index unfilled (-1: never)
 };
 
-constexpr int QUANT_ROWS = 64;                              // rows per unit
-constexpr int QUANT_CONSUMER_WARPS = 8;                     // 8 rows each, 4 lanes per row
+constexpr int QUANT_ROWS = 32;                              // rows per unit
+constexpr int QUANT_CONSUMER_WARPS = QUANT_ROWS / 8;        // 8 rows each, 4 lanes per row
 constexpr int QUANT_THREADS = (QUANT_CONSUMER_WARPS + 1) * 32;  // + the producer warp
-constexpr int QUANT_STAGES = 3;
-constexpr int QUANT_STAGE_BYTES = QUANT_ROWS * 128 * 2;     // 16 KB of BF16
+constexpr int QUANT_STAGES = 1;  // measured best: many small CTAs beat deep rings
+constexpr int QUANT_STAGE_BYTES = QUANT_ROWS * 128 * 2;     // 8 KB of BF16
 constexpr int QUANT_SMEM_BYTES = QUANT_STAGES * QUANT_STAGE_BYTES + 2 * QUANT_STAGES * 8 + 16;
 constexpr float QUANT_MIN_FAST_SCALE = 0x1p-40f;
 constexpr float QUANT_MIN_FAST_AMAX = 0x1p-100f;
@@ -237,8 +239,11 @@ __global__ void __launch_bounds__(QUANT_THREADS)
     __syncthreads();
 
     // With programmatic dependent launch the previous kernel of the stream may
-    // still be writing x or masked_m: wait for it before the first read.
+    // still be writing x or masked_m: wait for it before the first read.  The
+    // next kernel may start its own set-up as CTAs of this one finish (it
+    // waits for this grid's completion before it reads anything).
     griddep_wait();
+    griddep_launch_dependents();
     if (u_begin >= u_end) return;
 
     if (warp == QUANT_CONSUMER_WARPS) {
