@@ -418,6 +418,39 @@ def run_ours(args, ws, rank, local):
         torch.cuda.synchronize()
         per_shape_ms[i] = e0.elapsed_time(e1) / args.steps
 
+    # FP32-output calls on the tensor-bound problems (m = 4096): same inputs and
+    # copies, an FP32 D per copy, K launches back to back per problem
+    f32out = None
+    if not args.no_f32out:
+        f32_rows, f_tot, t_tot = [], 0.0, 0.0
+        for i, (m, n, k, copies) in enumerate(items):
+            if m != max(wl.DENSE_SWEEP_M):
+                continue
+            d32 = [torch.empty((m, n), dtype=torch.float32, device=dev) for _ in copies]
+            for r in range(len(copies)):  # warm-up
+                A, sA, B, sB, _ = copies[r]
+                fg.fg_gemm_fp8_nt_f32out(A, sA, B, sB, d32[r], stream=stream)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for r in range(args.steps):
+                A, sA, B, sB, _ = copies[r % len(copies)]
+                fg.fg_gemm_fp8_nt_f32out(A, sA, B, sB, d32[r % len(copies)], stream=stream)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            us = e0.elapsed_time(e1) * 1e3 / args.steps
+            f = 2.0 * m * n * k
+            f32_rows.append({"m": m, "n": n, "k": k, "us": round(us, 2), "tflops": round(f / us / 1e6, 1),
+                             "time_vs_bf16_out": round(us / (per_shape_ms[i] * 1e3), 3)})
+            f_tot += f
+            t_tot += us
+            del d32
+        st, det = fg.fg_get_device_status()
+        if st != 0:
+            raise RuntimeError(f"device status {st} detail {det:#x} after the FP32-output runs")
+        f32out = {"call": "fg_gemm_fp8_nt_f32out", "tflops_over_shapes": round(f_tot / t_tot / 1e6, 1),
+                  "timing": "K back-to-back launches per problem after the per-problem pass, same copies",
+                  "shapes": f32_rows}
+
     peaks, peak_src = load_peaks()
     fp8_peak = peaks["bf16_tflops"] * FP8_PER_BF16
     hbm_peak = peaks["hbm_gbs"]
@@ -583,7 +616,7 @@ def run_ours(args, ws, rank, local):
             "roofline": roofline, "roofline_other_kernels": others, "roofline_hbm": roofline_hbm,
             "shapes": shape_rows, "clocks": clock_info, "e2e": e2e,
             "gpu_launches": len(items) * args.steps, "cpu_baseline": cpu,
-            "quantize_per_token": quant,
+            "quantize_per_token": quant, "f32_output": f32out,
         }
         print(json.dumps(line), flush=True)
 
@@ -598,6 +631,7 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-quantize", action="store_true", help="skip the activation-quantization figures")
+    ap.add_argument("--no-f32out", action="store_true", help="skip the FP32-output figures")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     args = ap.parse_args(argv)
     if args.warmup < 3 and args.impl == "ours" and not args.shapes:

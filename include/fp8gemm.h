@@ -96,6 +96,26 @@ fg_status fg_grouped_gemm_fp8_masked(const void *A, int a_fmt, const float *sA, 
                                      const int32_t *masked_m, int G, int M_cap, int n, int k,
                                      void *stream);
 
+/* FP32-output forms of the three calls above (page whose first section is
+ * "从一张“算力账单”说起", section 4.2 "基础矩阵乘法的调用与验证": the output is
+ * BF16 by default, FP32 on request at some cost in speed).  Arguments,
+ * layouts, written rows and errors are those of the BF16 calls; D is float
+ * [rows][n] (masked: [G][M_cap][n]), 16-byte aligned, and receives the FP32
+ * result of the two-level accumulation without the final rounding to BF16
+ * (rounding it to BF16, nearest even, gives the BF16 call's result bit for
+ * bit).  Tile plans are chosen as for BF16 output. */
+fg_status fg_gemm_fp8_nt_f32out(const void *A, int a_fmt, const float *sA, int ld_sA,
+                                const void *B, int b_fmt, const float *sB,
+                                float *D, int m, int n, int k, void *stream);
+fg_status fg_grouped_gemm_fp8_contiguous_f32out(const void *A, int a_fmt, const float *sA, int ld_sA,
+                                                const void *B, int b_fmt, const float *sB, float *D,
+                                                const int32_t *m_indices, int M, int n, int k, int G,
+                                                void *stream);
+fg_status fg_grouped_gemm_fp8_masked_f32out(const void *A, int a_fmt, const float *sA, int ld_sA,
+                                            const void *B, int b_fmt, const float *sB, float *D,
+                                            const int32_t *masked_m, int G, int M_cap, int n, int k,
+                                            void *stream);
+
 /* Layout helper (the page's "LHS scales must be TMA-aligned and transposed",
  * section "基本用法"): src is row-major [batches][rows][kb], dst receives
  * [batches][kb][ld_dst] with ld_dst >= rows, ld_dst % 4 == 0; padding entries

@@ -12,7 +12,7 @@ Layouts (see the header for the full contract):
   sA  MN-major [ceil(k/128), ld] (masked: [G, ceil(k/128), ld]) float32
   B   [n, k] (grouped: [G, n, k])
   sB  [ceil(n/128), ceil(k/128)] (grouped: [G, ...]) float32
-  D   [m, n] (masked: [G, M_cap, n]) bfloat16
+  D   [m, n] (masked: [G, M_cap, n]) bfloat16; float32 for the *_f32out calls
 """
 from __future__ import annotations
 
@@ -40,6 +40,9 @@ SIGNATURES = {
     "fg_gemm_fp8_nt": (_I, [_P, _I, _P, _I, _P, _I, _P, _P, _I, _I, _I, _P]),
     "fg_grouped_gemm_fp8_contiguous": (_I, [_P, _I, _P, _I, _P, _I, _P, _P, _P, _I, _I, _I, _I, _P]),
     "fg_grouped_gemm_fp8_masked": (_I, [_P, _I, _P, _I, _P, _I, _P, _P, _P, _I, _I, _I, _I, _P]),
+    "fg_gemm_fp8_nt_f32out": (_I, [_P, _I, _P, _I, _P, _I, _P, _P, _I, _I, _I, _P]),
+    "fg_grouped_gemm_fp8_contiguous_f32out": (_I, [_P, _I, _P, _I, _P, _I, _P, _P, _P, _I, _I, _I, _I, _P]),
+    "fg_grouped_gemm_fp8_masked_f32out": (_I, [_P, _I, _P, _I, _P, _I, _P, _P, _P, _I, _I, _I, _I, _P]),
     "fg_scales_a_to_mn_major": (_I, [_P, _P, _I, _I, _I, _I, _P]),
     "fg_scales_a_ld": (_I, [_I]),
     "fg_quantize_fp8_per_token": (_I, [_P, _I, _I, _P, _P, _I, _P, _I, _I, _I, _P]),
@@ -130,51 +133,79 @@ def _cdiv(a, b):
 
 def fg_gemm_fp8_nt(A, sA, B, sB, D, *, a_fmt=None, b_fmt=None, stream=None):
     """Dense D[m,n] = A[m,k] . B[n,k]^T with 1x128 / 128x128 FP32 scales, BF16 out."""
+    return _dense("fg_gemm_fp8_nt", _BF16, A, sA, B, sB, D, a_fmt, b_fmt, stream)
+
+
+def fg_gemm_fp8_nt_f32out(A, sA, B, sB, D, *, a_fmt=None, b_fmt=None, stream=None):
+    """fg_gemm_fp8_nt with an FP32 D (the accumulator before BF16 rounding)."""
+    return _dense("fg_gemm_fp8_nt_f32out", _F32, A, sA, B, sB, D, a_fmt, b_fmt, stream)
+
+
+def _dense(name, d_dtypes, A, sA, B, sB, D, a_fmt, b_fmt, stream):
     _need(A, "A", _FP8, 2), _need(B, "B", _FP8, 2), _need(sA, "sA", _F32, 2)
-    _need(sB, "sB", _F32, 2), _need(D, "D", _BF16, 2)
+    _need(sB, "sB", _F32, 2), _need(D, "D", d_dtypes, 2)
     m, k = A.shape
     n = B.shape[0]
     if B.shape[1] != k or tuple(D.shape) != (m, n):
         raise ValueError(f"shape mismatch A{tuple(A.shape)} B{tuple(B.shape)} D{tuple(D.shape)}")
     if sA.shape[0] != _cdiv(k, 128) or tuple(sB.shape) != (_cdiv(n, 128), _cdiv(k, 128)):
         raise ValueError(f"scale shapes sA{tuple(sA.shape)} sB{tuple(sB.shape)} do not fit m={m} n={n} k={k}")
-    st = lib().fg_gemm_fp8_nt(A.data_ptr(), _fmt_of(A, a_fmt), sA.data_ptr(), sA.shape[1], B.data_ptr(),
+    st = getattr(lib(), name)(A.data_ptr(), _fmt_of(A, a_fmt), sA.data_ptr(), sA.shape[1], B.data_ptr(),
                               _fmt_of(B, b_fmt), sB.data_ptr(), D.data_ptr(), m, n, k, _stream_ptr(stream))
-    _check("fg_gemm_fp8_nt", st)
+    _check(name, st)
     return D
 
 
 def fg_grouped_gemm_fp8_contiguous(A, sA, B, sB, D, m_indices, *, a_fmt=None, b_fmt=None, stream=None):
     """Contiguous layout: row r of A multiplies B[m_indices[r]]; rows with -1 stay untouched."""
+    return _contiguous("fg_grouped_gemm_fp8_contiguous", _BF16, A, sA, B, sB, D, m_indices, a_fmt, b_fmt, stream)
+
+
+def fg_grouped_gemm_fp8_contiguous_f32out(A, sA, B, sB, D, m_indices, *, a_fmt=None, b_fmt=None, stream=None):
+    """fg_grouped_gemm_fp8_contiguous with an FP32 D."""
+    return _contiguous("fg_grouped_gemm_fp8_contiguous_f32out", _F32, A, sA, B, sB, D, m_indices, a_fmt, b_fmt,
+                       stream)
+
+
+def _contiguous(name, d_dtypes, A, sA, B, sB, D, m_indices, a_fmt, b_fmt, stream):
     _need(A, "A", _FP8, 2), _need(B, "B", _FP8, 3), _need(sA, "sA", _F32, 2)
-    _need(sB, "sB", _F32, 3), _need(D, "D", _BF16, 2), _need(m_indices, "m_indices", _I32, 1)
+    _need(sB, "sB", _F32, 3), _need(D, "D", d_dtypes, 2), _need(m_indices, "m_indices", _I32, 1)
     M, k = A.shape
     G, n, kb_ = B.shape
     if kb_ != k or tuple(D.shape) != (M, n) or m_indices.shape[0] != M:
         raise ValueError("shape mismatch")
     if sA.shape[0] != _cdiv(k, 128) or tuple(sB.shape) != (G, _cdiv(n, 128), _cdiv(k, 128)):
         raise ValueError("scale shapes do not fit")
-    st = lib().fg_grouped_gemm_fp8_contiguous(
+    st = getattr(lib(), name)(
         A.data_ptr(), _fmt_of(A, a_fmt), sA.data_ptr(), sA.shape[1], B.data_ptr(), _fmt_of(B, b_fmt),
         sB.data_ptr(), D.data_ptr(), m_indices.data_ptr(), M, n, k, G, _stream_ptr(stream))
-    _check("fg_grouped_gemm_fp8_contiguous", st)
+    _check(name, st)
     return D
 
 
 def fg_grouped_gemm_fp8_masked(A, sA, B, sB, D, masked_m, *, a_fmt=None, b_fmt=None, stream=None):
     """Masked layout: rows r < masked_m[g] of group g are written; the rest stay untouched."""
+    return _masked("fg_grouped_gemm_fp8_masked", _BF16, A, sA, B, sB, D, masked_m, a_fmt, b_fmt, stream)
+
+
+def fg_grouped_gemm_fp8_masked_f32out(A, sA, B, sB, D, masked_m, *, a_fmt=None, b_fmt=None, stream=None):
+    """fg_grouped_gemm_fp8_masked with an FP32 D."""
+    return _masked("fg_grouped_gemm_fp8_masked_f32out", _F32, A, sA, B, sB, D, masked_m, a_fmt, b_fmt, stream)
+
+
+def _masked(name, d_dtypes, A, sA, B, sB, D, masked_m, a_fmt, b_fmt, stream):
     _need(A, "A", _FP8, 3), _need(B, "B", _FP8, 3), _need(sA, "sA", _F32, 3)
-    _need(sB, "sB", _F32, 3), _need(D, "D", _BF16, 3), _need(masked_m, "masked_m", _I32, 1)
+    _need(sB, "sB", _F32, 3), _need(D, "D", d_dtypes, 3), _need(masked_m, "masked_m", _I32, 1)
     G, M_cap, k = A.shape
     Gb, n, kb_ = B.shape
     if Gb != G or kb_ != k or tuple(D.shape) != (G, M_cap, n) or masked_m.shape[0] != G:
         raise ValueError("shape mismatch")
     if tuple(sA.shape[:2]) != (G, _cdiv(k, 128)) or tuple(sB.shape) != (G, _cdiv(n, 128), _cdiv(k, 128)):
         raise ValueError("scale shapes do not fit")
-    st = lib().fg_grouped_gemm_fp8_masked(
+    st = getattr(lib(), name)(
         A.data_ptr(), _fmt_of(A, a_fmt), sA.data_ptr(), sA.shape[2], B.data_ptr(), _fmt_of(B, b_fmt),
         sB.data_ptr(), D.data_ptr(), masked_m.data_ptr(), G, M_cap, n, k, _stream_ptr(stream))
-    _check("fg_grouped_gemm_fp8_masked", st)
+    _check(name, st)
     return D
 
 

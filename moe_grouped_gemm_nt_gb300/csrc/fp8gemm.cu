@@ -191,15 +191,16 @@ struct Launcher {
     }
 };
 
-template <int BN, int STAGES, int KIND, bool SPLITK>
-using Kernel = Launcher<fg::fp8_gemm_kernel<BN, STAGES, KIND, SPLITK>, fg::SmemLayout<BN, STAGES>::BYTES, SPLITK>;
+template <int BN, int STAGES, int KIND, bool SPLITK, bool F32OUT = false>
+using Kernel =
+    Launcher<fg::fp8_gemm_kernel<BN, STAGES, KIND, SPLITK, F32OUT>, fg::SmemLayout<BN, STAGES>::BYTES, SPLITK>;
 
 // 256 x 256 tiles on CTA pairs: operand stages of 16 + 16 KB per CTA, and a
 // scale ring at least as deep (the producer issues both in the same iteration)
 constexpr int kPairStages = 5;
 constexpr int kPairScaleStages = 8;
-template <int KIND>
-using PairKernel = Launcher<fg::fp8_gemm_pair_kernel<KIND, kPairStages, kPairScaleStages>,
+template <int KIND, bool F32OUT = false>
+using PairKernel = Launcher<fg::fp8_gemm_pair_kernel<KIND, kPairStages, kPairScaleStages, F32OUT>,
                             fg::PairSmemLayout<kPairStages, kPairScaleStages>::BYTES, true>;
 
 // Tile plan of one call: output tile width and split-K factor.
@@ -305,9 +306,9 @@ bool use_pair(int kind, const Plan &plan, int rows) {
     return rows >= fg::PAIR_ROWS;
 }
 
-// Shared part of the three GEMM entry points.
+// Shared part of the GEMM entry points (BF16 or, with F32OUT, FP32 output).
 //   a_rows: rows of the 2-D A / D row space; b_rows: G * n.
-template <int KIND>
+template <int KIND, bool F32OUT = false>
 fg_status run(const void *A, int a_fmt, const float *sA, int ld_sA, const void *B, int b_fmt, const float *sB,
               void *D, const int32_t *m_indices, const int32_t *masked_m, int rows, int G, int n, int k,
               cudaStream_t stream) {
@@ -344,8 +345,10 @@ fg_status run(const void *A, int a_fmt, const float *sA, int ld_sA, const void *
                    fg::BLOCK_K, fg::BLOCK_M) ||
         !encode_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, (uint64_t)k, (uint64_t)G * n, (uint64_t)k, fg::BLOCK_K,
                    (uint32_t)(pair ? fg::PAIR_BN / 2 : BN)) ||
-        !encode_2d(&td, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, D, (uint64_t)n, (uint64_t)a_rows_total,
-                   (uint64_t)n * 2, 64, 32))
+        !(F32OUT ? encode_2d(&td, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, D, (uint64_t)n, (uint64_t)a_rows_total,
+                             (uint64_t)n * 4, 32, 32)
+                 : encode_2d(&td, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, D, (uint64_t)n, (uint64_t)a_rows_total,
+                             (uint64_t)n * 2, 64, 32)))
         return cuda_fail();
 
     GemmParams p{};
@@ -362,7 +365,7 @@ fg_status run(const void *A, int a_fmt, const float *sA, int ld_sA, const void *
     p.sB = sB;
     p.m_indices = m_indices;
     p.masked_m = masked_m;
-    p.D = static_cast<__nv_bfloat16 *>(D);
+    p.D = D;
     p.status = dev->status;
     p.timeout_ns = (unsigned long long)g_watchdog_ms.load() * 1000000ull;
     p.debug_skip_iter = g_debug_skip_iter.exchange(-1);
@@ -376,11 +379,11 @@ fg_status run(const void *A, int a_fmt, const float *sA, int ld_sA, const void *
             p.group_m = raster_group_m(KIND, (int)pblocks, 2 * k);
             p.idesc = fg::make_idesc_f8f6f4(fg::PAIR_ROWS, fg::PAIR_BN, (uint32_t)a_fmt, (uint32_t)b_fmt);
             const long long tiles = pblocks * p.num_n_blocks;
-            long long clusters = PairKernel<KIND>::max_active_clusters(2);
+            long long clusters = PairKernel<KIND, F32OUT>::max_active_clusters(2);
             if (clusters < 1) return cuda_fail();
             if (clusters > sms / 2) clusters = sms / 2;  // the SM limit (fg_set_num_sms); sms >= 2 here
             if (clusters > tiles) clusters = tiles;
-            return PairKernel<KIND>::launch(ta, tb, td, tsa, p, (int)(2 * clusters), 2, stream);
+            return PairKernel<KIND, F32OUT>::launch(ta, tb, td, tsa, p, (int)(2 * clusters), 2, stream);
         }
     }
     const long long max_tiles = m_blocks_total * p.num_n_blocks;
@@ -390,16 +393,17 @@ fg_status run(const void *A, int a_fmt, const float *sA, int ld_sA, const void *
             const long long grid = max_tiles * plan.split;
             if (grid > INT32_MAX) return FG_ERR_UNSUPPORTED;
             if (BN == 256)
-                return Kernel<256, 4, KIND, true>::launch(ta, tb, td, tsa, p, (int)grid, plan.split, stream);
-            return Kernel<128, 6, KIND, true>::launch(ta, tb, td, tsa, p, (int)grid, plan.split, stream);
+                return Kernel<256, 4, KIND, true, F32OUT>::launch(ta, tb, td, tsa, p, (int)grid, plan.split,
+                                                                  stream);
+            return Kernel<128, 6, KIND, true, F32OUT>::launch(ta, tb, td, tsa, p, (int)grid, plan.split, stream);
         }
         if (BN == 128) {
             const int grid = (int)(max_tiles < sms ? max_tiles : sms);
-            return Kernel<128, 6, KIND, false>::launch(ta, tb, td, tsa, p, grid, 1, stream);
+            return Kernel<128, 6, KIND, false, F32OUT>::launch(ta, tb, td, tsa, p, grid, 1, stream);
         }
     }
     const int grid = (int)(max_tiles < sms ? max_tiles : sms);
-    return Kernel<256, 4, KIND, false>::launch(ta, tb, td, tsa, p, grid, 1, stream);
+    return Kernel<256, 4, KIND, false, F32OUT>::launch(ta, tb, td, tsa, p, grid, 1, stream);
 }
 
 }  // namespace
@@ -448,6 +452,27 @@ fg_status fg_grouped_gemm_fp8_masked(const void *A, int a_fmt, const float *sA, 
                                      int M_cap, int n, int k, void *stream) {
     return run<fg::KIND_MASKED>(A, a_fmt, sA, ld_sA, B, b_fmt, sB, D, nullptr, masked_m, M_cap, G, n, k,
                                 static_cast<cudaStream_t>(stream));
+}
+
+fg_status fg_gemm_fp8_nt_f32out(const void *A, int a_fmt, const float *sA, int ld_sA, const void *B, int b_fmt,
+                                const float *sB, float *D, int m, int n, int k, void *stream) {
+    return run<fg::KIND_DENSE, true>(A, a_fmt, sA, ld_sA, B, b_fmt, sB, D, nullptr, nullptr, m, 1, n, k,
+                                     static_cast<cudaStream_t>(stream));
+}
+
+fg_status fg_grouped_gemm_fp8_contiguous_f32out(const void *A, int a_fmt, const float *sA, int ld_sA,
+                                                const void *B, int b_fmt, const float *sB, float *D,
+                                                const int32_t *m_indices, int M, int n, int k, int G,
+                                                void *stream) {
+    return run<fg::KIND_CONTIGUOUS, true>(A, a_fmt, sA, ld_sA, B, b_fmt, sB, D, m_indices, nullptr, M, G, n, k,
+                                          static_cast<cudaStream_t>(stream));
+}
+
+fg_status fg_grouped_gemm_fp8_masked_f32out(const void *A, int a_fmt, const float *sA, int ld_sA, const void *B,
+                                            int b_fmt, const float *sB, float *D, const int32_t *masked_m, int G,
+                                            int M_cap, int n, int k, void *stream) {
+    return run<fg::KIND_MASKED, true>(A, a_fmt, sA, ld_sA, B, b_fmt, sB, D, nullptr, masked_m, M_cap, G, n, k,
+                                      static_cast<cudaStream_t>(stream));
 }
 
 fg_status fg_scales_a_to_mn_major(const float *src, float *dst, int batches, int rows, int kb, int ld_dst,

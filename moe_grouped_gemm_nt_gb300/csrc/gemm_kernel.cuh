@@ -92,7 +92,7 @@ struct GemmParams {
     const float *sB;
     const int32_t *m_indices;
     const int32_t *masked_m;
-    __nv_bfloat16 *D;
+    void *D;           // bfloat16 [rows][n], or float [rows][n] for the FP32-output instantiations
     uint32_t *status;  // [0] first error code, [1] its detail
     unsigned long long timeout_ns;
     int debug_skip_iter;  // producer leaves this K iteration unarmed (-1: never)
@@ -257,10 +257,11 @@ __device__ __forceinline__ float ld_shared_f32(uint32_t addr) {
     return v;
 }
 
-// Tensor maps: A [rows][k] u8, B [G*n][k] u8, D [rows][n] bf16 (all 2-D, 128-byte
-// swizzle); SA over the MN-major LHS scales: 2-D {rows, kb} (dense, contiguous)
-// or 3-D {M_cap, kb, G} (masked), fp32, no swizzle, box of 128 rows.
-template <int BN, int STAGES, int KIND, bool SPLITK>
+// Tensor maps: A [rows][k] u8, B [G*n][k] u8, D [rows][n] bf16 or (F32OUT) fp32
+// (all 2-D, 128-byte swizzle; D boxes of 32 rows x 128 bytes); SA over the
+// MN-major LHS scales: 2-D {rows, kb} (dense, contiguous) or 3-D {M_cap, kb, G}
+// (masked), fp32, no swizzle, box of 128 rows.
+template <int BN, int STAGES, int KIND, bool SPLITK, bool F32OUT>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                     const __grid_constant__ CUtensorMap tmap_d, const __grid_constant__ CUtensorMap tmap_sa,
@@ -558,6 +559,29 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 use_tma = __all_sync(0xffffffffu, row_ok);
             if (use_tma) {
                 const bool rows_in = (KIND != KIND_DENSE) || (sub * 32 < ti.row_limit);
+                if constexpr (F32OUT) {
+                    // FP32 boxes: 32 rows x 32 columns (128 bytes per row, same swizzle)
+#pragma unroll
+                    for (int bx = 0; bx < COLS / 32; ++bx) {
+                        const int x = col0 + bx * 32;
+                        if (!rows_in || x >= p.n) continue;  // box entirely outside D: nothing to write
+                        if (lane == 0) bulk_wait_group_read<0>();  // staging buffer free again
+                        __syncwarp();
+#pragma unroll
+                        for (int ch = 0; ch < 8; ++ch) {
+                            const float *f = acc + bx * 32 + ch * 4;
+                            const uint32_t off = (uint32_t)lane * 128u + ((uint32_t)(ch ^ (lane & 7)) << 4);
+                            st_shared_v4(stg + off, __float_as_uint(f[0]), __float_as_uint(f[1]),
+                                         __float_as_uint(f[2]), __float_as_uint(f[3]));
+                        }
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            tma_store_2d(&tmap_d, stg, x, d_row);
+                            bulk_commit_group();
+                        }
+                    }
+                } else {
 #pragma unroll
                 for (int bx = 0; bx < COLS / 64; ++bx) {
                     const int x = col0 + bx * 64;
@@ -578,15 +602,31 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         bulk_commit_group();
                     }
                 }
+                }
             } else if (row_ok) {
-                __nv_bfloat16 *drow = p.D + (size_t)(d_row + lane) * p.n;
+                if constexpr (F32OUT) {
+                    float *drow = static_cast<float *>(p.D) + (size_t)(d_row + lane) * p.n;
 #pragma unroll
-                for (int ch = 0; ch < COLS / 8; ++ch) {
-                    const int c = col0 + ch * 8;
-                    if (c < p.n) {
-                        const float *f = acc + ch * 8;
-                        st_global_v4(drow + c, pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]),
-                                     pack_bf16x2(f[4], f[5]), pack_bf16x2(f[6], f[7]));
+                    for (int ch = 0; ch < COLS / 8; ++ch) {
+                        const int c = col0 + ch * 8;
+                        if (c < p.n) {
+                            const float *f = acc + ch * 8;
+                            st_global_v4(drow + c, __float_as_uint(f[0]), __float_as_uint(f[1]),
+                                         __float_as_uint(f[2]), __float_as_uint(f[3]));
+                            st_global_v4(drow + c + 4, __float_as_uint(f[4]), __float_as_uint(f[5]),
+                                         __float_as_uint(f[6]), __float_as_uint(f[7]));
+                        }
+                    }
+                } else {
+                    __nv_bfloat16 *drow = static_cast<__nv_bfloat16 *>(p.D) + (size_t)(d_row + lane) * p.n;
+#pragma unroll
+                    for (int ch = 0; ch < COLS / 8; ++ch) {
+                        const int c = col0 + ch * 8;
+                        if (c < p.n) {
+                            const float *f = acc + ch * 8;
+                            st_global_v4(drow + c, pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]),
+                                         pack_bf16x2(f[4], f[5]), pack_bf16x2(f[6], f[7]));
+                        }
                     }
                 }
             }
@@ -652,10 +692,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                     sum.w += v[u][q].w;
                                 }
                             }
-                            uint2 w;
-                            w.x = pack_bf16x2(sum.x, sum.y);
-                            w.y = pack_bf16x2(sum.z, sum.w);
-                            *reinterpret_cast<uint2 *>(p.D + (size_t)(ti.a_row + row[u]) * p.n + col[u]) = w;
+                            const size_t d_off = (size_t)(ti.a_row + row[u]) * p.n + col[u];
+                            if constexpr (F32OUT) {
+                                *reinterpret_cast<float4 *>(static_cast<float *>(p.D) + d_off) = sum;
+                            } else {
+                                uint2 w;
+                                w.x = pack_bf16x2(sum.x, sum.y);
+                                w.y = pack_bf16x2(sum.z, sum.w);
+                                *reinterpret_cast<uint2 *>(static_cast<__nv_bfloat16 *>(p.D) + d_off) = w;
+                            }
                         }
                     }
                 }

@@ -114,9 +114,9 @@ __device__ __forceinline__ PairTile get_pair_tile(const GemmParams &p, int t, in
 }
 
 // Tensor maps: A [rows][k] u8 (box 128 rows), B [G*n][k] u8 (box 128 rows: one
-// CTA's half of the pair tile's 256), D [rows][n] bf16, SA as for the one-CTA
-// kernel.  Launched with clusters of 2 CTAs.
-template <int KIND, int STAGES, int SS>
+// CTA's half of the pair tile's 256), D [rows][n] bf16 or (F32OUT) fp32, SA as
+// for the one-CTA kernel.  Launched with clusters of 2 CTAs.
+template <int KIND, int STAGES, int SS, bool F32OUT>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     fp8_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                          const __grid_constant__ CUtensorMap tmap_d, const __grid_constant__ CUtensorMap tmap_sa,
@@ -374,6 +374,29 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             else
                 use_tma = __all_sync(0xffffffffu, row_ok);
             if (use_tma) {
+                if constexpr (F32OUT) {
+                    // FP32 boxes: 32 rows x 32 columns (128 bytes per row, same swizzle)
+#pragma unroll
+                    for (int bx = 0; bx < COLS / 32; ++bx) {
+                        const int x = col0 + bx * 32;
+                        if (!rows_in || x >= p.n) continue;  // box entirely outside D: nothing to write
+                        if (lane == 0) bulk_wait_group_read<0>();  // staging buffer free again
+                        __syncwarp();
+#pragma unroll
+                        for (int ch = 0; ch < 8; ++ch) {
+                            const float *f = acc + bx * 32 + ch * 4;
+                            const uint32_t off = (uint32_t)lane * 128u + ((uint32_t)(ch ^ (lane & 7)) << 4);
+                            st_shared_v4(stg + off, __float_as_uint(f[0]), __float_as_uint(f[1]),
+                                         __float_as_uint(f[2]), __float_as_uint(f[3]));
+                        }
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            tma_store_2d(&tmap_d, stg, x, d_row);
+                            bulk_commit_group();
+                        }
+                    }
+                } else {
 #pragma unroll
                 for (int bx = 0; bx < COLS / 64; ++bx) {
                     const int x = col0 + bx * 64;
@@ -394,15 +417,31 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         bulk_commit_group();
                     }
                 }
+                }
             } else if (row_ok) {
-                __nv_bfloat16 *drow = p.D + (size_t)(d_row + lane) * p.n;
+                if constexpr (F32OUT) {
+                    float *drow = static_cast<float *>(p.D) + (size_t)(d_row + lane) * p.n;
 #pragma unroll
-                for (int ch = 0; ch < COLS / 8; ++ch) {
-                    const int c = col0 + ch * 8;
-                    if (c < p.n) {
-                        const float *f = acc + ch * 8;
-                        st_global_v4(drow + c, pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]),
-                                     pack_bf16x2(f[4], f[5]), pack_bf16x2(f[6], f[7]));
+                    for (int ch = 0; ch < COLS / 8; ++ch) {
+                        const int c = col0 + ch * 8;
+                        if (c < p.n) {
+                            const float *f = acc + ch * 8;
+                            st_global_v4(drow + c, __float_as_uint(f[0]), __float_as_uint(f[1]),
+                                         __float_as_uint(f[2]), __float_as_uint(f[3]));
+                            st_global_v4(drow + c + 4, __float_as_uint(f[4]), __float_as_uint(f[5]),
+                                         __float_as_uint(f[6]), __float_as_uint(f[7]));
+                        }
+                    }
+                } else {
+                    __nv_bfloat16 *drow = static_cast<__nv_bfloat16 *>(p.D) + (size_t)(d_row + lane) * p.n;
+#pragma unroll
+                    for (int ch = 0; ch < COLS / 8; ++ch) {
+                        const int c = col0 + ch * 8;
+                        if (c < p.n) {
+                            const float *f = acc + ch * 8;
+                            st_global_v4(drow + c, pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]),
+                                         pack_bf16x2(f[4], f[5]), pack_bf16x2(f[6], f[7]));
+                        }
                     }
                 }
             }

@@ -119,3 +119,23 @@ def test_quantize_argument_checks():
     assert call(k=128 * 65536, ld_x=128 * 65536) == 3  # more K blocks than a grid dimension holds
     assert call(batches=65536) == 3
     assert call(rows=0) == 0              # nothing to do: no launch
+
+
+def test_f32out_argument_checks():
+    """The FP32-output calls share the BF16 calls' host-side checks."""
+    L = fg.lib()
+    ok = dict(A=FAKE, a_fmt=0, sA=FAKE, ld=128, B=FAKE, b_fmt=0, sB=FAKE, D=FAKE, m=128, n=256, k=512)
+
+    def dense(**kw):
+        a = dict(ok, **kw)
+        return L.fg_gemm_fp8_nt_f32out(a["A"], a["a_fmt"], a["sA"], a["ld"], a["B"], a["b_fmt"], a["sB"],
+                                       a["D"], a["m"], a["n"], a["k"], None)
+
+    assert dense(D=None) == 1 and dense(a_fmt=3) == 1 and dense(n=0) == 1
+    assert dense(D=FAKE + 8) == 2 and dense(ld=130) == 2
+    assert dense(k=520) == 3 and dense(n=260) == 3
+    assert dense(m=0) == 0  # nothing to do: no launch
+    assert L.fg_grouped_gemm_fp8_contiguous_f32out(FAKE, 0, FAKE, 200, FAKE, 0, FAKE, FAKE, FAKE, 200, 64, 128, 2,
+                                                   None) == 3
+    assert L.fg_grouped_gemm_fp8_masked_f32out(FAKE, 0, FAKE, 256, FAKE, 0, FAKE, FAKE, None, 2, 256, 64, 128,
+                                               None) == 1
