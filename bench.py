@@ -279,6 +279,93 @@ def measure_quantize(fg, torch, dev, stream, hbm_peak, peak_src, reps=20, traffi
             "shapes": rows_out}
 
 
+def measure_other_configs(fg, torch, dev, stream, fp8_peak, hbm_peak, peak_src, reps=10):
+    """Throughput of the other workloads (the parity tests cover their results):
+    contiguous G in {4, 8} x 8192 rows per group, masked G in {1, 2, 4, 16} with
+    capacity 256 and seeded uniform counts, and the large square problems
+    (8192^3, k = 8192 + 384, E5M2 B).  Operands are drawn on the device from a
+    seeded generator (N(0,1) x 64 clipped to the E4M3 range: the timing does not
+    depend on the values); scales uniform in [0.5, 1.5], log-uniform in
+    [2^-8, 2^8] for the square problems.  Each problem rotates over copies of
+    its inputs and output larger than twice L2, `reps` back-to-back launches
+    between CUDA events."""
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(wl.seed_for(5))
+
+    def f8(shape, dt=torch.float8_e4m3fn):
+        lim = 448.0 if dt == torch.float8_e4m3fn else 57344.0
+        return (torch.randn(shape, device=dev, generator=gen) * 64).clamp(-lim, lim).to(dt)
+
+    def unif(shape):
+        return torch.rand(shape, device=dev, generator=gen) + 0.5
+
+    def logu(shape):
+        return torch.exp2(torch.rand(shape, device=dev, generator=gen) * 16 - 8)
+
+    def timed(fn, copies):
+        for c in copies[:2]:
+            fn(*c)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for r in range(reps):
+            fn(*copies[r % len(copies)])
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) * 1e3 / reps
+
+    def row(name, us, flops, byts):
+        return {"problem": name, "us": round(us, 2), "tflops": round(flops / us / 1e6, 1),
+                "gbs": round(byts / us / 1e3, 1), "frac_fp8_peak": round(flops / us / 1e6 / fp8_peak, 3),
+                "frac_hbm_peak": round(byts / us / 1e3 / hbm_peak, 3)}
+
+    out = {"contiguous": [], "masked": [], "large_dense": []}
+    for (G, n, k) in wl.contiguous_shapes():
+        M = G * wl.CONTIGUOUS_ROWS_PER_GROUP
+        kb, nb = (k + 127) // 128, (n + 127) // 128
+        byts = M * k + G * n * k + M * n * 2
+        nc = max(2, -(-ROTATE_BYTES // byts))
+        mi = torch.arange(G, device=dev, dtype=torch.int32).repeat_interleave(wl.CONTIGUOUS_ROWS_PER_GROUP)
+        copies = [(f8((M, k)), unif((kb, M)), f8((G, n, k)), unif((G, nb, kb)),
+                   torch.empty((M, n), dtype=torch.bfloat16, device=dev), mi) for _ in range(nc)]
+        us = timed(lambda *c: fg.fg_grouped_gemm_fp8_contiguous(*c, stream=stream), copies)
+        out["contiguous"].append(row(f"G={G} M={M} n={n} k={k}", us, 2.0 * M * n * k, byts))
+        del copies
+    for (G, n, k) in wl.masked_shapes():
+        Mc = wl.MASKED_M_CAP
+        kb, nb = (k + 127) // 128, (n + 127) // 128
+        rng = wl.rng_for(wl.seed_for(3, wl.masked_shapes().index((G, n, k))))
+        counts = rng.integers(0, Mc, size=G, endpoint=True).astype(np.int32)
+        valid, used = int(counts.sum()), int((counts > 0).sum())
+        byts = valid * k + used * n * k + valid * n * 2
+        full = G * Mc * k + G * n * k + G * Mc * n * 2
+        nc = max(2, -(-ROTATE_BYTES // full))
+        mm = torch.from_numpy(counts).to(dev)
+        copies = [(f8((G, Mc, k)), unif((G, kb, Mc)), f8((G, n, k)), unif((G, nb, kb)),
+                   torch.empty((G, Mc, n), dtype=torch.bfloat16, device=dev), mm) for _ in range(nc)]
+        us = timed(lambda *c: fg.fg_grouped_gemm_fp8_masked(*c, stream=stream), copies)
+        r = row(f"G={G} M_cap={Mc} n={n} k={k} valid_rows={valid}", us, 2.0 * valid * n * k, byts)
+        out["masked"].append(r)
+        del copies
+    for (m, n, k, bfmt) in wl.large_dense_shapes():
+        kb, nb = (k + 127) // 128, (n + 127) // 128
+        bdt = torch.float8_e4m3fn if bfmt == wl.E4M3 else torch.float8_e5m2
+        byts = m * k + n * k + m * n * 2
+        nc = max(2, -(-ROTATE_BYTES // byts))
+        copies = [(f8((m, k)), logu((kb, m)), f8((n, k), bdt), logu((nb, kb)),
+                   torch.empty((m, n), dtype=torch.bfloat16, device=dev)) for _ in range(nc)]
+        us = timed(lambda *c: fg.fg_gemm_fp8_nt(*c, stream=stream), copies)
+        out["large_dense"].append(row(f"{m}x{n}x{k} B={'E5M2' if bfmt else 'E4M3'}", us, 2.0 * m * n * k, byts))
+        del copies
+    st, det = fg.fg_get_device_status()
+    if st != 0:
+        raise RuntimeError(f"device status {st} detail {det:#x} after the other workloads")
+    out["timing"] = (f"{reps} back-to-back launches per problem between CUDA events, rotating copies "
+                     ">= 272 MiB, after the GEMM steps; masked GB/s and TFLOP/s count valid rows only")
+    out["peak_source"] = peak_src
+    return out
+
+
 def run_reference(args, ws, rank):
     if rank != 0:
         return
@@ -508,6 +595,10 @@ def run_ours(args, ws, rank, local):
                         "timing": "per-problem back-to-back launches after the timed steps",
                         "peak_source": f"{peak_src}: hbm copy"}
 
+    others_cfg = None
+    if not args.no_other_configs:
+        others_cfg = measure_other_configs(fg, torch, dev, stream, fp8_peak, hbm_peak, peak_src)
+
     quant = None
     if not args.no_quantize:
         quant = measure_quantize(fg, torch, dev, stream, hbm_peak, peak_src, traffic_tab=traffic_tab)
@@ -616,7 +707,7 @@ def run_ours(args, ws, rank, local):
             "roofline": roofline, "roofline_other_kernels": others, "roofline_hbm": roofline_hbm,
             "shapes": shape_rows, "clocks": clock_info, "e2e": e2e,
             "gpu_launches": len(items) * args.steps, "cpu_baseline": cpu,
-            "quantize_per_token": quant, "f32_output": f32out,
+            "quantize_per_token": quant, "f32_output": f32out, "other_workloads": others_cfg,
         }
         print(json.dumps(line), flush=True)
 
@@ -632,6 +723,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-quantize", action="store_true", help="skip the activation-quantization figures")
     ap.add_argument("--no-f32out", action="store_true", help="skip the FP32-output figures")
+    ap.add_argument("--no-other-configs", action="store_true",
+                    help="skip the contiguous, masked and large-square throughput figures")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     args = ap.parse_args(argv)
     if args.warmup < 3 and args.impl == "ours" and not args.shapes:
