@@ -186,12 +186,14 @@ fg_status fg_query_dense_plan(int m, int n, int k, int *block_n, int *split_k);
 fg_status fg_query_dense_plan_ex(int m, int n, int k, int *block_n, int *split_k, int *cta_pair);
 
 /* CTA-pair tiles for later calls: -1 (default) where they apply (persistent
- * 256-wide plans of the dense and masked layouts with at least 256 rows, no
- * forced plan), 0 never, 1 for every persistent 256-wide dense or masked plan.
- * The contiguous layout always uses 128-row tiles (two adjacent 128-row blocks
- * may belong to two groups; measured, pairing them with a second pass for
- * such blocks was slower than 128-row tiles).  Results differ between the
- * modes only by FP32 summation order; FG_ERR_INVALID_ARG for other values. */
+ * 256-wide dense plans with at least 256 rows, no forced plan), 0 never, 1 for
+ * every persistent 256-wide dense or masked plan.  The contiguous layout
+ * always uses 128-row tiles (two adjacent 128-row blocks may belong to two
+ * groups; measured, pairing them with a second pass for such blocks was
+ * slower than 128-row tiles).  The masked layout uses 128-row tiles unless
+ * the mode is 1 (a 256-row tile also computes a group's empty rows past its
+ * count; measured slower).  Results differ between the modes only by FP32
+ * summation order; FG_ERR_INVALID_ARG for other values. */
 fg_status fg_set_pair_mode(int mode);
 
 /* Programmatic dependent launch of the GEMM kernels (default on): a call's
