@@ -232,3 +232,32 @@ def test_graph_replays_quantize_and_masked_gemm_with_new_counts():
             if c:
                 compare(got[gi, :c], ref[gi, :c], what=f"graph replay group {gi}")
     assert fg.fg_get_device_status()[0] == fg.FG_OK
+
+
+@pytest.mark.parametrize("fmt", [wl.E4M3, wl.E5M2])
+def test_quantize_exact_ties(fmt):
+    """Rows whose quotients x / s land exactly on FP8 midpoints (ties to even),
+    with scales s = odd * 2^j whose reciprocals are inexact in FP32: a quotient
+    that is not the correctly rounded one breaks such a tie.  Each row holds
+    amax = fmax * s (so s is exact) and x = M * s for midpoints M, all exact in
+    BF16; the fast division path (s >= 2^-40) and the IEEE fallback are both
+    exercised."""
+    t = oracle.decode_table(fmt)
+    fmax = 448.0 if fmt == wl.E4M3 else 57344.0
+    vals = sorted({float(v) for v in t[:128] if np.isfinite(v) and v >= 0})
+    mids = [(a + b) / 2 for a, b in zip(vals[:-1], vals[1:])]
+    rows = []
+    for odd in (3, 5, 7, 11, 13, 25, 49):
+        for j in (-60, -20, -3, 0, 7, 20):
+            s = odd * 2.0 ** j
+            amax = fmax * s
+            xs = [m * s for m in mids]
+            cand = np.array([amax] + xs + [-x for x in xs], np.float64).astype(np.float32)
+            exact = torch.from_numpy(cand).to(torch.bfloat16).to(torch.float32).numpy() == cand
+            if not exact[0]:
+                continue
+            row = cand[exact][:128]
+            rows.append(np.pad(row, (0, 128 - row.size)))
+    x = np.stack(rows).astype(np.float32)
+    A, sA = _run(x, fmt)
+    _check_against_oracle(x, fmt, A, sA)

@@ -550,3 +550,20 @@ def test_quantize_closed_forms(fmt):
             # half a step, plus the float32 rounding of the division
             assert np.all(np.abs(d - v) <= step / 2 + np.abs(v) * 2.0 ** -23)
             assert np.all((np.sign(d) == np.sign(v)) | (d == 0))
+
+
+def test_quantize_divides_rather_than_multiplying_by_the_reciprocal():
+    """An exact FP8 tie after the division, which multiplying by a rounded
+    reciprocal misses.  amax = 3136 gives s = 3136 / 448 = 7 exactly;
+    x = 12.6875 (BF16: 1100.1011b) gives x / s = 1.8125 exactly, the midpoint
+    between the E4M3 values 1.75 and 1.875, which rounds to the even code
+    0x3E (1.75).  With 1/7 rounded to float (0.14285715) the product is
+    1.8125001, above the midpoint: code 0x3F."""
+    x = np.zeros((1, 128), np.float32)
+    x[0, 0] = 3136.0
+    x[0, 1] = 12.6875
+    x[0, 2] = -12.6875
+    q, s = oracle.quantize_per_token(x, oracle.E4M3)
+    assert s[0, 0] == 7.0
+    assert q[0, 1] == 0x3E and q[0, 2] == 0xBE
+    assert q[0, 0] == 0x7E
