@@ -139,3 +139,29 @@ def test_f32out_argument_checks():
                                                    None) == 3
     assert L.fg_grouped_gemm_fp8_masked_f32out(FAKE, 0, FAKE, 256, FAKE, 0, FAKE, FAKE, None, 2, 256, 64, 128,
                                                None) == 1
+
+
+def test_binding_rejects_host_tensors_and_wrong_dtypes():
+    """The Python binding checks tensors before it calls the library: host
+    tensors, wrong dtypes and shape mismatches raise (no CUDA call needed)."""
+    import torch
+
+    x_host = torch.zeros((4, 128), dtype=torch.bfloat16)
+    with pytest.raises(TypeError):
+        fg.fg_quantize_fp8_per_token(x_host)  # not a CUDA tensor
+    with pytest.raises(TypeError):
+        fg.fg_quantize_fp8_per_token(torch.zeros((4, 128), dtype=torch.float32))
+    a = torch.zeros((4, 128), dtype=torch.uint8)
+    s = torch.zeros((1, 4), dtype=torch.float32)
+    d16 = torch.zeros((4, 8), dtype=torch.bfloat16)
+    d32 = torch.zeros((4, 8), dtype=torch.float32)
+    b = torch.zeros((8, 128), dtype=torch.uint8)
+    sb = torch.zeros((1, 1), dtype=torch.float32)
+    with pytest.raises(ValueError):
+        fg.fg_gemm_fp8_nt(a, s, b, sb, d16)  # host tensors
+    with pytest.raises(ValueError):
+        fg.fg_gemm_fp8_nt_f32out(a, s, b, sb, d32)
+    with pytest.raises(ValueError):
+        fg.fg_grouped_gemm_fp8_masked_f32out(a.view(1, 4, 128), s.view(1, 1, 4), b.view(1, 8, 128),
+                                             sb.view(1, 1, 1), d32.view(1, 4, 8),
+                                             torch.zeros(1, dtype=torch.int32))
