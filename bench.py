@@ -108,6 +108,20 @@ def load_traffic():
     return out
 
 
+def bench_config(ws):
+    """The `config` object of the JSON line: the same for both arms, so that the
+    reference arm (the CPU oracle) is read as a run of the same workload."""
+    return {"workload": WORKLOAD, "problems_per_step": len(wl.DENSE_SWEEP_M) * len(wl.DENSE_SWEEP_NK),
+            "l2": ("inputs larger than L2: each problem rotates over identical copies of its "
+                   "inputs and output totalling >= 272 MiB (> 2 x L2)"),
+            "timing": ("CUDA events on the launching stream around K back-to-back steps; a step "
+                       "launches every problem once, grouped by kernel instantiation with an event "
+                       "at each group boundary (per-kernel device time); the per-problem table comes "
+                       "from K launches of each problem captured in a CUDA graph and replayed after "
+                       "the timed steps"),
+            "parallelism": f"replica x{ws} (independent problems per GPU)"}
+
+
 def problem_bytes(m, n, k):
     kb, nb = (k + 127) // 128, (n + 127) // 128
     return m * k + n * k + m * kb * 4 + nb * kb * 4 + m * n * 2
@@ -396,8 +410,9 @@ def run_reference(args, ws, rank):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": float(np.mean(times)) * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "fp8_e4m3",
         "data": "synthetic (seeded N(0,1), quantized to E4M3)",
-        "config": {"workload": WORKLOAD, "l2": "n/a (CPU)"},
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+        "config": bench_config(ws),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": sample + "; host cores, no GPU involved (L2 rotation does not apply)"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -700,15 +715,7 @@ def run_ours(args, ws, rank, local):
             "warmup": args.warmup, "ms_per_step": round(step_ms, 4), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "fp8_e4m3",
             "data": "synthetic (seeded N(0,1), quantized to E4M3 per 1x128 / 128x128 group)",
-            "config": {"workload": WORKLOAD, "problems_per_step": len(items),
-                       "l2": ("inputs larger than L2: each problem rotates over identical copies of its "
-                              "inputs and output totalling >= 272 MiB (> 2 x L2)"),
-                       "timing": ("CUDA events on the launching stream around K back-to-back steps; a step "
-                                  "launches every problem once, grouped by kernel instantiation with an event "
-                                  "at each group boundary (per-kernel device time); the per-problem table comes "
-                                  "from K launches of each problem captured in a CUDA graph and replayed after "
-                                  "the timed steps"),
-                       "parallelism": f"replica x{ws} (independent problems per GPU)"},
+            "config": dict(bench_config(ws), problems_per_step=len(items)),
             "hbm_gbs": round(ws * bytes_step / (step_ms * 1e-3) / 1e9, 1),
             "wall_ms_per_step": round(wall / args.steps * 1e3, 3),
             "roofline": roofline, "roofline_other_kernels": others, "roofline_hbm": roofline_hbm,

@@ -78,7 +78,11 @@ fg_status fg_gemm_fp8_nt(const void *A, int a_fmt, const float *sA, int ld_sA,
  * either the group id of the tile's first row or -1 (padding).  Rows whose id
  * equals the tile's group are written with A[r] x B[g]^T; all other rows of D
  * are left untouched.  A tile whose first id is outside [0, G) is skipped (and
- * recorded as FG_ERR_DEVICE_CHECK unless it is -1).  M % 128 == 0. */
+ * recorded as FG_ERR_DEVICE_CHECK unless it is -1).  Input that breaks the
+ * alignment contract is reported, never computed: a row whose id is neither
+ * -1 nor its tile's group, or a group id inside a tile whose first row is -1,
+ * is left untouched and recorded as FG_ERR_DEVICE_CHECK with the row index as
+ * the detail.  M % 128 == 0. */
 fg_status fg_grouped_gemm_fp8_contiguous(const void *A, int a_fmt, const float *sA, int ld_sA,
                                          const void *B, int b_fmt, const float *sB, void *D,
                                          const int32_t *m_indices, int M, int n, int k, int G,
@@ -160,6 +164,13 @@ int fg_scales_a_ld(int rows);
  * 2 MMA, 3 epilogue) in bits 24..31; for FG_ERR_DEVICE_CHECK the offending
  * group or tile index. */
 fg_status fg_get_device_status(void *stream, uint32_t *detail);
+
+/* Tuning and testing knobs.  fg_set_num_sms, fg_set_config_override,
+ * fg_set_pair_mode, fg_set_programmatic_launch and fg_set_watchdog_ms set
+ * PROCESS-WIDE state: each applies to every later call from any thread, on any
+ * device and stream, until it is set again.  Threads that want different
+ * settings must serialize their set-and-call sequences themselves; a call
+ * reads each setting once, when it starts. */
 
 /* Limit the number of SMs (persistent CTAs) used by later calls on any device
  * ("SM资源控制"); 0 restores the default (all SMs). */

@@ -98,6 +98,42 @@ def _stream_ptr(stream):
     return int(stream)
 
 
+def _common_device(tensors, stream=None):
+    """The one CUDA device that every operand of a call lives on.
+
+    The library launches on the calling thread's current device, so operands on
+    another device (or spread over several) would be handed to kernels of the
+    wrong GPU: raise instead.  A torch stream must belong to that device too; a
+    raw stream handle (an int) cannot be checked and is taken as given."""
+    dev = None
+    for name, t in tensors:
+        if t is None:
+            continue
+        d = t.device
+        if dev is None:
+            dev = d
+        elif d != dev:
+            raise ValueError(f"{name} is on {d}, but the other operands are on {dev}")
+    if dev is not None and stream is not None and hasattr(stream, "device") and stream.device != dev:
+        raise ValueError(f"stream belongs to {stream.device}, but the operands are on {dev}")
+    return dev
+
+
+def _launch(name, tensors, stream, *args):
+    """Call the C entry point `name` with `args` (the stream handle appended),
+    on the device of `tensors`: when that is not the current device, it is made
+    current for the duration of the call."""
+    dev = _common_device(tensors, stream)
+    f = getattr(lib(), name)
+    if dev is not None and dev.index is not None and dev.index != torch.cuda.current_device():
+        with torch.cuda.device(dev):
+            s = _stream_ptr(stream if stream is not None else torch.cuda.current_stream(dev))
+            st = f(*args, s)
+    else:
+        st = f(*args, _stream_ptr(stream))
+    _check(name, st)
+
+
 def _fmt_of(t, fmt):
     if fmt is not None:
         return int(fmt)
@@ -150,9 +186,9 @@ def _dense(name, d_dtypes, A, sA, B, sB, D, a_fmt, b_fmt, stream):
         raise ValueError(f"shape mismatch A{tuple(A.shape)} B{tuple(B.shape)} D{tuple(D.shape)}")
     if sA.shape[0] != _cdiv(k, 128) or tuple(sB.shape) != (_cdiv(n, 128), _cdiv(k, 128)):
         raise ValueError(f"scale shapes sA{tuple(sA.shape)} sB{tuple(sB.shape)} do not fit m={m} n={n} k={k}")
-    st = getattr(lib(), name)(A.data_ptr(), _fmt_of(A, a_fmt), sA.data_ptr(), sA.shape[1], B.data_ptr(),
-                              _fmt_of(B, b_fmt), sB.data_ptr(), D.data_ptr(), m, n, k, _stream_ptr(stream))
-    _check(name, st)
+    _launch(name, (("A", A), ("sA", sA), ("B", B), ("sB", sB), ("D", D)), stream,
+            A.data_ptr(), _fmt_of(A, a_fmt), sA.data_ptr(), sA.shape[1], B.data_ptr(), _fmt_of(B, b_fmt),
+            sB.data_ptr(), D.data_ptr(), m, n, k)
     return D
 
 
@@ -176,10 +212,9 @@ def _contiguous(name, d_dtypes, A, sA, B, sB, D, m_indices, a_fmt, b_fmt, stream
         raise ValueError("shape mismatch")
     if sA.shape[0] != _cdiv(k, 128) or tuple(sB.shape) != (G, _cdiv(n, 128), _cdiv(k, 128)):
         raise ValueError("scale shapes do not fit")
-    st = getattr(lib(), name)(
-        A.data_ptr(), _fmt_of(A, a_fmt), sA.data_ptr(), sA.shape[1], B.data_ptr(), _fmt_of(B, b_fmt),
-        sB.data_ptr(), D.data_ptr(), m_indices.data_ptr(), M, n, k, G, _stream_ptr(stream))
-    _check(name, st)
+    _launch(name, (("A", A), ("sA", sA), ("B", B), ("sB", sB), ("D", D), ("m_indices", m_indices)), stream,
+            A.data_ptr(), _fmt_of(A, a_fmt), sA.data_ptr(), sA.shape[1], B.data_ptr(), _fmt_of(B, b_fmt),
+            sB.data_ptr(), D.data_ptr(), m_indices.data_ptr(), M, n, k, G)
     return D
 
 
@@ -202,10 +237,9 @@ def _masked(name, d_dtypes, A, sA, B, sB, D, masked_m, a_fmt, b_fmt, stream):
         raise ValueError("shape mismatch")
     if tuple(sA.shape[:2]) != (G, _cdiv(k, 128)) or tuple(sB.shape) != (G, _cdiv(n, 128), _cdiv(k, 128)):
         raise ValueError("scale shapes do not fit")
-    st = getattr(lib(), name)(
-        A.data_ptr(), _fmt_of(A, a_fmt), sA.data_ptr(), sA.shape[2], B.data_ptr(), _fmt_of(B, b_fmt),
-        sB.data_ptr(), D.data_ptr(), masked_m.data_ptr(), G, M_cap, n, k, _stream_ptr(stream))
-    _check(name, st)
+    _launch(name, (("A", A), ("sA", sA), ("B", B), ("sB", sB), ("D", D), ("masked_m", masked_m)), stream,
+            A.data_ptr(), _fmt_of(A, a_fmt), sA.data_ptr(), sA.shape[2], B.data_ptr(), _fmt_of(B, b_fmt),
+            sB.data_ptr(), D.data_ptr(), masked_m.data_ptr(), G, M_cap, n, k)
     return D
 
 
@@ -229,9 +263,8 @@ def fg_scales_a_to_mn_major(src, dst=None, *, stream=None):
         if tuple(dst.shape[:-1]) != shape[:-1] or dst.shape[-1] < rows:
             raise ValueError("dst shape does not fit")
         ld = dst.shape[-1]
-    st = lib().fg_scales_a_to_mn_major(src.data_ptr(), dst.data_ptr(), batches, rows, kb, ld,
-                                        _stream_ptr(stream))
-    _check("fg_scales_a_to_mn_major", st)
+    _launch("fg_scales_a_to_mn_major", (("src", src), ("dst", dst)), stream,
+            src.data_ptr(), dst.data_ptr(), batches, rows, kb, ld)
     return dst
 
 
@@ -277,9 +310,8 @@ def fg_quantize_fp8_per_token(X, A=None, sA=None, *, fmt=E4M3, masked_m=None, st
         if masked_m.shape[0] != batches:
             raise ValueError("masked_m must hold one count per batch")
         mp = masked_m.data_ptr()
-    st = lib().fg_quantize_fp8_per_token(X.data_ptr(), ld_x, int(fmt), A.data_ptr(), sA.data_ptr(),
-                                         sA.shape[-1], mp, batches, rows, k, _stream_ptr(stream))
-    _check("fg_quantize_fp8_per_token", st)
+    _launch("fg_quantize_fp8_per_token", (("X", X), ("A", A), ("sA", sA), ("masked_m", masked_m)), stream,
+            X.data_ptr(), ld_x, int(fmt), A.data_ptr(), sA.data_ptr(), sA.shape[-1], mp, batches, rows, k)
     return A, sA
 
 

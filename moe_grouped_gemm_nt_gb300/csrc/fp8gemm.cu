@@ -30,7 +30,11 @@ std::atomic<int> g_num_sms_override{0};
 std::atomic<uint32_t> g_watchdog_ms{kDefaultWatchdogMs};
 std::atomic<int> g_debug_skip_iter{-1};
 
+// Per-device facts read once.  `ready` is published with release after the
+// other fields are written, and read with acquire, so a thread that sees it
+// set also sees the status address and the SM count.
 struct DeviceInfo {
+    std::atomic<int> ready{0};
     int num_sms = 0;
     uint32_t *status = nullptr;
 };
@@ -43,15 +47,16 @@ fg_status device_info(DeviceInfo **out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return cuda_fail();
     DeviceInfo &d = g_dev[dev];
-    if (d.num_sms == 0) {
+    if (!d.ready.load(std::memory_order_acquire)) {
         std::lock_guard<std::mutex> lock(g_dev_mutex);
-        if (d.num_sms == 0) {
+        if (!d.ready.load(std::memory_order_relaxed)) {
             int sms = 0;
             void *st = nullptr;
             if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return cuda_fail();
             if (cudaGetSymbolAddress(&st, g_status) != cudaSuccess) return cuda_fail();
             d.status = static_cast<uint32_t *>(st);
             d.num_sms = sms;
+            d.ready.store(1, std::memory_order_release);
         }
     }
     *out = &d;

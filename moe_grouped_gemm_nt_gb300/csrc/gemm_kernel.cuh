@@ -471,16 +471,31 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         for (int t = t_begin; t < num_tiles && ok; t += t_step) {
             const Tile ti = get_tile<BN, KIND>(p, t, m_blocks);
             if (!ti.valid) {
-                if (KIND == KIND_CONTIGUOUS && ti.group != -1 && warp == 0 && lane == 0)
-                    record_error(p, DEV_ERR_CHECK, (uint32_t)t);
+                if constexpr (KIND == KIND_CONTIGUOUS) {
+                    // a skipped block must be all padding (-1 rows); a group id
+                    // elsewhere in it breaks the 128-row alignment contract
+                    if (ti.group != -1) {
+                        if (warp == 0 && lane == 0) record_error(p, DEV_ERR_CHECK, (uint32_t)t);
+                    } else if (half == 0 && ti.n_blk == 0) {
+                        const int gid = __ldg(p.m_indices + ti.a_row + r);
+                        if (gid != -1) record_error(p, DEV_ERR_CHECK, (uint32_t)(ti.a_row + r));
+                    }
+                }
                 continue;
             }
             // which rows of this warp are written
             bool row_ok;
-            if constexpr (KIND == KIND_CONTIGUOUS)
-                row_ok = __ldg(p.m_indices + ti.a_row + r) == ti.group;
-            else
+            if constexpr (KIND == KIND_CONTIGUOUS) {
+                // rows of the tile's group are written, -1 rows are padding; any
+                // other id breaks the 128-row alignment contract (not written,
+                // reported with the row index)
+                const int gid = __ldg(p.m_indices + ti.a_row + r);
+                row_ok = gid == ti.group;
+                if (gid != ti.group && gid != -1 && half == 0)
+                    record_error(p, DEV_ERR_CHECK, (uint32_t)(ti.a_row + r));
+            } else {
                 row_ok = r < ti.row_limit;
+            }
             const int col0 = ti.n_blk * BN + half * COLS;
 
             uint64_t acc2[COLS / 2];  // FP32 running sums, packed in pairs of columns
@@ -639,7 +654,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (split > 1) {
             // every CTA of the cluster takes both barriers, whatever happened above
             cluster_sync();
-            const bool tile_ok = t_begin < num_tiles && !*abort_flag;
+            // a rank whose watchdog fired left its partial incomplete: then no
+            // rank writes D (the status word already records the timeout)
+            bool any_abort = false;
+            for (uint32_t q = 0; q < split; ++q)
+                any_abort |= ld_shared_cluster_u32(map_shared_rank(smem_u32((const void *)abort_flag), q)) != 0u;
+            const bool tile_ok = t_begin < num_tiles && !any_abort;
             if (tile_ok && warp < NUM_EPI_WARPS) {
                 const Tile ti = get_tile<BN, KIND>(p, t_begin, m_blocks);
                 if (ti.valid) {

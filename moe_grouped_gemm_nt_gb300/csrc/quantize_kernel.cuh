@@ -132,7 +132,7 @@ __device__ __forceinline__ float div_by_const(float a, float b, float yb) {
     return __fmaf_rn(__fmaf_rn(-q, b, a), yb, q);
 }
 
-// A walk over consecutive units (K block fastest, then 64-row block, then
+// A walk over consecutive units (K block fastest, then 32-row block, then
 // batch) with the batch's valid rows.  next() is only called while units
 // remain, so the batch index never passes the last batch.
 struct QuantWalk {
@@ -281,7 +281,7 @@ __global__ void __launch_bounds__(QUANT_THREADS)
     }
 
     // -------------------------------------------------------------- consumers
-    const int lrow = warp * 8 + (lane >> 2);  // row of the unit, 0..63
+    const int lrow = warp * 8 + (lane >> 2);  // row of the unit, 0..QUANT_ROWS-1
     const int jq = lane & 3;                  // columns 32 c' + 8 jq .. + 7 for chunks c' = c ^ (lrow & 1)
     const int flip = lrow & 1;
     constexpr float kFmax = FMT == 0 ? 448.f : 57344.f;

@@ -165,3 +165,23 @@ def test_binding_rejects_host_tensors_and_wrong_dtypes():
         fg.fg_grouped_gemm_fp8_masked_f32out(a.view(1, 4, 128), s.view(1, 1, 4), b.view(1, 8, 128),
                                              sb.view(1, 1, 1), d32.view(1, 4, 8),
                                              torch.zeros(1, dtype=torch.int32))
+
+
+def test_binding_rejects_operands_on_different_devices():
+    """The library launches on the current device, so the binding refuses
+    operands spread over two devices, and a torch stream of another device
+    (checked on stand-ins that carry only a device attribute: no GPU needed)."""
+    from types import SimpleNamespace
+
+    import torch
+
+    d0, d1 = torch.device("cuda", 0), torch.device("cuda", 1)
+    t0, t1 = SimpleNamespace(device=d0), SimpleNamespace(device=d1)
+    assert fg._common_device((("A", t0), ("B", t0), ("D", t0))) == d0
+    assert fg._common_device((("A", t1), ("masked_m", None), ("D", t1))) == d1
+    with pytest.raises(ValueError, match="D is on cuda:1"):
+        fg._common_device((("A", t0), ("B", t0), ("D", t1)))
+    with pytest.raises(ValueError, match="stream belongs to cuda:1"):
+        fg._common_device((("A", t0), ("D", t0)), stream=SimpleNamespace(device=d1))
+    # a raw stream handle cannot be checked and is accepted as given
+    assert fg._common_device((("A", t0),), stream=12345) == d0

@@ -89,6 +89,36 @@ def test_contiguous_bad_group_id_reports_device_check():
     compare(got[:128], ref[:128], what="valid part")
 
 
+@pytest.mark.parametrize("case", ["foreign_id_in_tile", "id_in_skipped_block"])
+def test_contiguous_misaligned_segments_report_device_check(case):
+    """Rows that break the 128-row segment contract are never written and the
+    call reports FG_ERR_DEVICE_CHECK with the offending row: a row of another
+    group inside a tile, or a group id inside a block whose first row is -1."""
+    p = wl.contiguous([128, 100], n=64, k=256, seed=43)
+    mi = p.m_indices.copy()
+    if case == "foreign_id_in_tile":
+        bad = 5
+        mi[bad] = 1          # tile 0 belongs to group 0
+    else:
+        mi[128:] = -1
+        bad = 130
+        mi[bad] = 1          # the block starting at row 128 is skipped
+    D = torch.full((p.M, p.n), -1, dtype=torch.int16, device="cuda").view(torch.bfloat16)
+    fg.fg_grouped_gemm_fp8_contiguous(dev(p.A, fp8_dtype(0)), fg.fg_scales_a_to_mn_major(dev(p.sA)),
+                                      dev(p.B, fp8_dtype(0)), dev(p.sB), D, dev(mi))
+    st, detail = fg.fg_get_device_status()
+    assert st == 6 and detail == bad
+    got = d_to_bits(D)
+    assert np.all(got[bad] == SENTINEL)
+    init = np.full((p.M, p.n), SENTINEL, np.uint16)
+    mi_ref = mi.copy()
+    mi_ref[bad] = -1  # what the kernel writes: the contract-breaking row stays untouched
+    ref, _ = oracle.grouped_contiguous(p.A, 0, p.sA, p.B, 0, p.sB, mi_ref, init)
+    written = mi_ref >= 0
+    assert np.array_equal(got[~written], ref[~written])
+    compare(got[written], ref[written], what=f"contiguous {case}")
+
+
 @pytest.mark.parametrize("G,n,k", wl.contiguous_shapes())
 def test_contiguous_workload(G, n, k):
     """G groups of 8192 rows, (n,k) weight shapes, sampled outputs."""
