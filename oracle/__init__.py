@@ -14,6 +14,10 @@ the header of ``oracle.c``:
   sections "基本用法" and "两级精度累加与细粒度缩放".
 * ``grouped_contiguous``     -- same page, "连续布局分组GEMM".
 * ``grouped_masked``         -- same page, "掩码布局分组GEMM".
+* ``k_grouped``              -- the same scaled NT product with the groups
+  concatenated along K (one K segment per group, the weight-gradient step of
+  MoE training; a reading of the same page's "DeepGEMM提供三种FP8GEMM实现",
+  which names the grouped kinds by the training forward pass).
 * ``decode`` / ``bf16_rne``  -- FP8 decoding and FP64 -> bfloat16 rounding.
 * ``encode_fp8``             -- float32 -> FP8 code, nearest even, saturating.
 * ``quantize_per_token``     -- 1x128 activation quantization producing the
@@ -83,6 +87,10 @@ def _load():
         lib.oracle_grouped_masked.argtypes = [P, I, P, P, I, P, P, I, I, I, I, P, P]
         lib.oracle_grouped_masked_at.restype = I
         lib.oracle_grouped_masked_at.argtypes = [P, I, P, P, I, P, P, I, I, I, I, LL, P, P, P, P, P]
+        lib.oracle_k_grouped.restype = I
+        lib.oracle_k_grouped.argtypes = [P, I, P, P, I, P, P, I, I, I, I, P, P]
+        lib.oracle_k_grouped_at.restype = I
+        lib.oracle_k_grouped_at.argtypes = [P, I, P, P, I, P, P, I, I, I, I, LL, P, P, P, P, P]
         lib.oracle_encode_fp8.restype = I
         lib.oracle_encode_fp8.argtypes = [I, ctypes.c_float]
         lib.oracle_quantize_per_token.restype = I
@@ -258,4 +266,37 @@ def grouped_masked_at(A, a_fmt, sA, B, b_fmt, sB, masked_m, groups, rows, cols):
                                           _ptr(rows), _ptr(cols), _ptr(d64), _ptr(d16))
     if rc != 0:
         raise ValueError(f"oracle_grouped_masked_at failed: {rc}")
+    return d16, d64
+
+
+def k_grouped(A, a_fmt, sA, B, b_fmt, sB, ks, want_f64=True):
+    """K-grouped NT GEMM.  A [M,K] u8, sA [M,ceil(K/128)], B [N,K] u8,
+    sB [ceil(N/128),ceil(K/128)], ks [G] int32 segment lengths (multiples of
+    128, sum <= K).  Returns (D bf16 bits [G,M,N], D f64 [G,M,N] or None)."""
+    A, B, sA, sB, ks = _u8(A), _u8(B), _f32(sA), _f32(sB), _i32(ks)
+    M, K = A.shape
+    N = B.shape[0]
+    G = ks.size
+    assert B.shape == (N, K) and sA.shape == (M, _num_kb(K)) and sB.shape == ((N + 127) // 128, _num_kb(K))
+    d16 = np.empty((G, M, N), np.uint16)
+    d64 = np.empty((G, M, N), np.float64) if want_f64 else None
+    rc = _load().oracle_k_grouped(_ptr(A), a_fmt, _ptr(sA), _ptr(B), b_fmt, _ptr(sB), _ptr(ks), G, M, N, K,
+                                  _ptr(d64), _ptr(d16))
+    if rc != 0:
+        raise ValueError(f"oracle_k_grouped failed: {rc}")
+    return d16, d64
+
+
+def k_grouped_at(A, a_fmt, sA, B, b_fmt, sB, ks, groups, rows, cols):
+    """K-grouped NT GEMM at sampled (groups[i], rows[i], cols[i]).  Returns (bf16 bits, f64)."""
+    A, B, sA, sB, ks = _u8(A), _u8(B), _f32(sA), _f32(sB), _i32(ks)
+    groups, rows, cols = _i64(groups), _i64(rows), _i64(cols)
+    M, K = A.shape
+    N = B.shape[0]
+    d16 = np.empty(rows.shape, np.uint16)
+    d64 = np.empty(rows.shape, np.float64)
+    rc = _load().oracle_k_grouped_at(_ptr(A), a_fmt, _ptr(sA), _ptr(B), b_fmt, _ptr(sB), _ptr(ks), ks.size, M, N,
+                                     K, rows.size, _ptr(groups), _ptr(rows), _ptr(cols), _ptr(d64), _ptr(d16))
+    if rc != 0:
+        raise ValueError(f"oracle_k_grouped_at failed: {rc}")
     return d16, d64

@@ -338,6 +338,96 @@ int oracle_grouped_masked_at(const uint8_t *A, int a_fmt, const float *sA,
     return 0;
 }
 
+/* ------------------------------------------------ K-grouped layout */
+
+/* Groups concatenated along K: the weight-gradient step of MoE training
+ * contracts over tokens, and each expert's tokens form one segment of the K
+ * axis (the pages name the grouped kinds by the training forward pass and
+ * inference; this is the same scaled NT product with the K range restricted
+ * per group).  A: [M][K] bytes and B: [N][K] bytes, both K-major, shared by all
+ * groups; sA: [M][ceil(K/128)] and sB: [ceil(N/128)][ceil(K/128)] row-major, the
+ * scaling of the NT GEMM.  Group g covers the K columns
+ * [off_g, off_g + ks[g]) with off_g = ks[0] + ... + ks[g-1]; every ks[g] is a
+ * multiple of 128 (so K blocks and scale blocks never straddle two groups) and
+ * their sum is at most K.  Output D [G][M][N]:
+ *
+ *   D[g][m][n] = sum over the K blocks kb of segment g of
+ *                sA[m,kb] * sB[n/128,kb] * sum_{k in kb} dec(A[m,k]) * dec(B[n,k])
+ *
+ * (an empty segment gives 0).  Returns -3 for sizes that break those rules. */
+static double k_segment_element(const uint8_t *a_row, const float *sa_row, const uint8_t *b_row,
+                                const float *sb_row, int kb0, int kb1, int K, const double *ta,
+                                const double *tb) {
+    double acc = 0.0;
+    for (int kb = kb0; kb < kb1; ++kb) {
+        int k0 = kb * ORACLE_KBLOCK;
+        int k1 = k0 + ORACLE_KBLOCK < K ? k0 + ORACLE_KBLOCK : K;
+        double partial = 0.0;
+        for (int kk = k0; kk < k1; ++kk) partial += ta[a_row[kk]] * tb[b_row[kk]];
+        acc += ((double)sa_row[kb] * (double)sb_row[kb]) * partial;
+    }
+    return acc;
+}
+
+static int k_segments_ok(const int32_t *ks, int G, int K) {
+    long long total = 0;
+    for (int g = 0; g < G; ++g) {
+        if (ks[g] < 0 || ks[g] % ORACLE_KBLOCK != 0) return 0;
+        total += ks[g];
+    }
+    return total <= K;
+}
+
+int oracle_k_grouped(const uint8_t *A, int a_fmt, const float *sA, const uint8_t *B, int b_fmt,
+                     const float *sB, const int32_t *ks, int G, int M, int N, int K,
+                     double *D64, uint16_t *D16) {
+    double ta[256], tb[256];
+    int num_kb = (K + ORACLE_KBLOCK - 1) / ORACLE_KBLOCK;
+    if (!shapes_ok(M, N, K) || G < 1 || fill_table(a_fmt, ta) || fill_table(b_fmt, tb)) return -1;
+    if (!k_segments_ok(ks, G, K)) return -3;
+    int off = 0;
+    for (int g = 0; g < G; ++g) {
+        int kb0 = off / ORACLE_KBLOCK, kb1 = (off + ks[g]) / ORACLE_KBLOCK;
+        off += ks[g];
+#pragma omp parallel for schedule(dynamic, 1)
+        for (long long r = 0; r < M; ++r) {
+            for (int c = 0; c < N; ++c) {
+                double v = k_segment_element(A + r * K, sA + r * num_kb, B + (long long)c * K,
+                                             sB + (long long)(c / ORACLE_NBLOCK) * num_kb, kb0, kb1, K, ta, tb);
+                long long o = ((long long)g * M + r) * N + c;
+                if (D64) D64[o] = v;
+                if (D16) D16[o] = oracle_bf16_rne(v);
+            }
+        }
+    }
+    return 0;
+}
+
+/* Sampled form over (g, m, n) triples. */
+int oracle_k_grouped_at(const uint8_t *A, int a_fmt, const float *sA, const uint8_t *B, int b_fmt,
+                        const float *sB, const int32_t *ks, int G, int M, int N, int K, long long count,
+                        const long long *groups, const long long *rows, const long long *cols,
+                        double *D64, uint16_t *D16) {
+    double ta[256], tb[256];
+    int num_kb = (K + ORACLE_KBLOCK - 1) / ORACLE_KBLOCK;
+    if (!shapes_ok(M, N, K) || G < 1 || fill_table(a_fmt, ta) || fill_table(b_fmt, tb)) return -1;
+    if (!k_segments_ok(ks, G, K)) return -3;
+    for (long long i = 0; i < count; ++i)
+        if (groups[i] < 0 || groups[i] >= G || rows[i] < 0 || rows[i] >= M || cols[i] < 0 || cols[i] >= N)
+            return -2;
+#pragma omp parallel for schedule(dynamic, 64)
+    for (long long i = 0; i < count; ++i) {
+        long long g = groups[i], r = rows[i], c = cols[i];
+        int off = 0;
+        for (long long h = 0; h < g; ++h) off += ks[h];
+        double v = k_segment_element(A + r * K, sA + r * num_kb, B + c * K, sB + (c / ORACLE_NBLOCK) * num_kb,
+                                     off / ORACLE_KBLOCK, (off + ks[g]) / ORACLE_KBLOCK, K, ta, tb);
+        if (D64) D64[i] = v;
+        if (D16) D16[i] = oracle_bf16_rne(v);
+    }
+    return 0;
+}
+
 /* ------------------------------------------- per-token FP8 quantization */
 
 /* FP8 code of the float v rounded to nearest, ties to even, saturating at the

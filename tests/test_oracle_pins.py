@@ -567,3 +567,84 @@ def test_quantize_divides_rather_than_multiplying_by_the_reciprocal():
     assert s[0, 0] == 7.0
     assert q[0, 1] == 0x3E and q[0, 2] == 0xBE
     assert q[0, 0] == 0x7E
+
+
+# ----------------------------------------------------------- K-grouped layout
+
+def _k_problem(M, N, K, seed):
+    p = wl.dense(M, N, K, seed=seed)
+    return p.A, p.sA, p.B, p.sB
+
+
+def test_k_grouped_unit_scales_equal_numpy_segment_matmuls():
+    """Unit scales reduce each group to a plain matmul over its K segment:
+    D[g] = dec(A[:, seg_g]) dec(B[:, seg_g])^T, exact in FP64 for E4M3 (numpy's
+    float64 matmul on column slices is the independent reference; a wrong
+    segment offset, a segment that runs over all of K, or an off-by-one K
+    block all change the result)."""
+    A, sA, B, sB = _k_problem(9, 140, 896, seed=41)
+    ks = np.array([256, 0, 128, 384], np.int32)    # 768 of the 896 columns; the last 128 belong to no group
+    _, d64 = oracle.k_grouped(A, 0, np.ones_like(sA), B, 0, np.ones_like(sB), ks)
+    a, b = _dec(A, 0), _dec(B, 0)
+    off = 0
+    for g, kg in enumerate(ks):
+        ref = a[:, off:off + kg] @ b[:, off:off + kg].T
+        assert np.array_equal(d64[g], ref), g
+        off += kg
+    assert np.all(d64[1] == 0.0)
+
+
+def test_k_grouped_equals_dense_on_segment_slices():
+    """With general scales, group g equals the dense definition applied to the
+    column slice of A and B and the matching columns of sA and sB (bitwise:
+    the same block sums in the same order)."""
+    A, sA, B, sB = _k_problem(12, 300, 1024, seed=42)
+    ks = np.array([384, 128, 512], np.int32)
+    d16, d64 = oracle.k_grouped(A, 0, sA, B, 0, sB, ks)
+    off = 0
+    for g, kg in enumerate(ks):
+        b0, b1 = off // 128, (off + kg) // 128
+        e16, e64 = oracle.gemm_fp8_nt(A[:, off:off + kg], 0, sA[:, b0:b1], B[:, off:off + kg], 0, sB[:, b0:b1])
+        assert np.array_equal(d64[g], e64) and np.array_equal(d16[g], e16), g
+        off += kg
+
+
+def test_k_grouped_groups_sum_to_the_full_k_product():
+    """Segments that tile all of K: the sum over groups is the dense result
+    over the whole K (power-of-two scales keep every term exact in FP64)."""
+    rng = np.random.default_rng(43)
+    A, _, B, _ = _k_problem(8, 130, 640, seed=43)
+    sA = np.exp2(rng.integers(-4, 5, size=(8, 5))).astype(np.float32)
+    sB = np.exp2(rng.integers(-4, 5, size=(2, 5))).astype(np.float32)
+    ks = np.array([128, 256, 0, 256], np.int32)
+    _, d64 = oracle.k_grouped(A, 0, sA, B, 0, sB, ks)
+    _, full = oracle.gemm_fp8_nt(A, 0, sA, B, 0, sB)
+    assert np.array_equal(d64.sum(axis=0), full)
+
+
+def test_k_grouped_one_hot_scale_picks_the_segment_block():
+    """sA zero except one K block (scale 2^3) inside group 1's segment: only
+    group 1 is nonzero, and it equals 8 x the unit-scale product of that one
+    block -- a shifted segment or scale index would select another block."""
+    A, _, B, _ = _k_problem(6, 64, 640, seed=44)
+    sA = np.zeros((6, 5), np.float32)
+    sA[:, 3] = 8.0
+    sB = np.ones((1, 5), np.float32)
+    ks = np.array([256, 256, 128], np.int32)        # group 1 = K blocks 2 and 3
+    _, d64 = oracle.k_grouped(A, 0, sA, B, 0, sB, ks)
+    ref = 8.0 * (_dec(A, 0)[:, 384:512] @ _dec(B, 0)[:, 384:512].T)
+    assert np.array_equal(d64[1], ref)
+    assert np.all(d64[0] == 0.0) and np.all(d64[2] == 0.0)
+
+
+def test_k_grouped_sampled_equals_full_and_bad_segments_are_refused():
+    A, sA, B, sB = _k_problem(10, 72, 512, seed=45)
+    ks = np.array([128, 256, 128], np.int32)
+    d16, d64 = oracle.k_grouped(A, 0, sA, B, 0, sB, ks)
+    rng = np.random.default_rng(0)
+    g, r, c = rng.integers(0, 3, 50), rng.integers(0, 10, 50), rng.integers(0, 72, 50)
+    s16, s64 = oracle.k_grouped_at(A, 0, sA, B, 0, sB, ks, g, r, c)
+    assert np.array_equal(s16, d16[g, r, c]) and np.array_equal(s64, d64[g, r, c])
+    for bad in ([100, 128], [-128, 256], [256, 384]):      # not a multiple of 128; negative; more than K
+        with pytest.raises(ValueError):
+            oracle.k_grouped(A, 0, sA, B, 0, sB, np.array(bad, np.int32))
