@@ -111,10 +111,13 @@ def run_masked(p: wl.Masked, D=None):
 
 
 def sample_positions(rows: int, cols: int, seed: int, block_m=128, block_n=256, n_rows_full=16,
-                     per_tile=1):
+                     per_tile=1, boundary_tiles=False):
     """Sampled output positions for large problems: `per_tile` random elements of
     every 128 x 256 output tile, the four corners of every tile, and every
-    column of `n_rows_full` random rows (including the first and the last)."""
+    column of `n_rows_full` random rows (including the first and the last).
+    With `boundary_tiles`, also every element of the four corner tiles and of
+    the boundary tiles (the last 128-row block across all columns and the
+    last 256-column block across all rows), each position once."""
     rng = np.random.default_rng(seed)
     rr, cc = [], []
     for t0 in range(0, rows, block_m):
@@ -127,4 +130,22 @@ def sample_positions(rows: int, cols: int, seed: int, block_m=128, block_n=256, 
     for r in full:
         rr += [int(r)] * cols
         cc += list(range(cols))
-    return np.array(rr, np.int64), np.array(cc, np.int64)
+    r = np.array(rr, np.int64)
+    c = np.array(cc, np.int64)
+    if boundary_tiles:
+        lm0 = (rows - 1) // block_m * block_m   # first row of the last 128-row block
+        ln0 = (cols - 1) // block_n * block_n   # first column of the last 256-column block
+        blocks = [
+            (0, min(block_m, rows), 0, min(block_n, cols)),   # top-left corner tile
+            (0, min(block_m, rows), ln0, cols),               # top-right corner tile
+            (lm0, rows, 0, cols),                              # last row block: bottom corners and edge
+            (0, rows, ln0, cols),                              # last column block: right corners and edge
+        ]
+        for (a0, a1, b0, b1) in blocks:
+            gr, gc = np.meshgrid(np.arange(a0, a1, dtype=np.int64), np.arange(b0, b1, dtype=np.int64),
+                                 indexing="ij")
+            r = np.concatenate([r, gr.ravel()])
+            c = np.concatenate([c, gc.ravel()])
+        lin = np.unique(r * cols + c)
+        r, c = lin // cols, lin % cols
+    return r, c

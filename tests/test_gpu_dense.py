@@ -82,7 +82,7 @@ def test_large_square_loguniform_scales(m, n, k, b_fmt):
     log-uniform in [2^-8, 2^8] to stress the FP32 promotion."""
     p = wl.dense(m, n, k, seed=wl.seed_for(4, int(k != 8192) + 2 * b_fmt), b_fmt=b_fmt, scales="loguniform")
     g = d_to_bits(run_dense(p))
-    rows, cols = sample_positions(m, n, seed=k + b_fmt, n_rows_full=4)
+    rows, cols = sample_positions(m, n, seed=k + b_fmt, n_rows_full=4, boundary_tiles=True)
     ref16, _ = oracle.gemm_fp8_nt_at(p.A, 0, p.sA, p.B, b_fmt, p.sB, rows, cols)
     compare(g[rows, cols], ref16, what=f"dense {m}x{n}x{k} b_fmt={b_fmt} (sampled)")
 

@@ -125,7 +125,7 @@ def test_contiguous_workload(G, n, k):
     p = wl.contiguous([wl.CONTIGUOUS_ROWS_PER_GROUP] * G, n=n, k=k,
                       seed=wl.seed_for(2, wl.contiguous_shapes().index((G, n, k))))
     got = d_to_bits(run_contiguous(p))
-    rows, cols = sample_positions(p.M, n, seed=G + n, n_rows_full=8)
+    rows, cols = sample_positions(p.M, n, seed=G + n, n_rows_full=8, boundary_tiles=True)
     ref, _ = oracle.grouped_contiguous_at(p.A, 0, p.sA, p.B, 0, p.sB, p.m_indices, rows, cols)
     compare(got[rows, cols], ref, what=f"contiguous G={G} n={n} k={k} (sampled)")
 

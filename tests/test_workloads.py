@@ -137,3 +137,25 @@ def test_cuda_library_does_not_use_the_oracle():
                 assert "oracle" not in imps and "workloads" not in imps, p
             if f.endswith((".cu", ".cuh", ".h", ".cpp")):
                 assert "oracle" not in open(p).read().lower(), p
+
+
+def test_sample_positions_cover_boundary_tiles():
+    """The sampled check of the largest problems covers every element of the
+    four corner tiles and of the last row block and last column block (the
+    tiles where partial-tile and clipping logic lives), each position once, and
+    at least one element of every other tile."""
+    import sys
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    from gpu_common import sample_positions
+
+    rows, cols = 1000, 700   # ragged in both directions: last blocks of 104 rows, 188 columns
+    r, c = sample_positions(rows, cols, seed=3, n_rows_full=2, boundary_tiles=True)
+    lin = r * cols + c
+    assert np.unique(lin).size == lin.size
+    hit = np.zeros((rows, cols), bool)
+    hit[r, c] = True
+    assert hit[896:, :].all() and hit[:, 512:].all()      # last row block, last column block
+    assert hit[:128, :256].all()                           # top-left corner tile
+    for t0 in range(0, rows, 128):
+        for c0 in range(0, cols, 256):
+            assert hit[t0:t0 + 128, c0:c0 + 256].any()
