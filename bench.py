@@ -381,6 +381,20 @@ def measure_other_configs(fg, torch, dev, stream, fp8_peak, hbm_peak, peak_src, 
         us = timed(fg.fg_gemm_fp8_nt, copies)
         out["large_dense"].append(row(f"{m}x{n}x{k} B={'E5M2' if bfmt else 'E4M3'}", us, 2.0 * m * n * k, byts))
         del copies
+    # K-grouped (the weight gradient of the contiguous workload): G segments of
+    # 8192 tokens, D [G][M][N] in BF16
+    out["k_grouped"] = []
+    for (G, M, N, tok) in wl.k_grouped_shapes():
+        K = G * tok
+        kb, nb = (K + 127) // 128, (N + 127) // 128
+        byts = M * K + N * K + G * M * N * 2
+        nc = max(2, -(-ROTATE_BYTES // byts))
+        ks = torch.full((G,), tok, dtype=torch.int32, device=dev)
+        copies = [(f8((M, K)), unif((kb, M)), f8((N, K)), unif((nb, kb)),
+                   torch.empty((G, M, N), dtype=torch.bfloat16, device=dev), ks) for _ in range(nc)]
+        us = timed(fg.fg_k_grouped_gemm_fp8_nt, copies)
+        out["k_grouped"].append(row(f"G={G} M={M} N={N} K={K} ({tok} tokens per group)", us, 2.0 * M * N * K, byts))
+        del copies
     st, det = fg.fg_get_device_status()
     if st != 0:
         raise RuntimeError(f"device status {st} detail {det:#x} after the other workloads")

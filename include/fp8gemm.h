@@ -120,6 +120,38 @@ fg_status fg_grouped_gemm_fp8_masked_f32out(const void *A, int a_fmt, const floa
                                             const int32_t *masked_m, int G, int M_cap, int n, int k,
                                             void *stream);
 
+/* K-grouped GEMM: groups concatenated along K, one NT product per group over
+ * its own segment of the K axis -- the weight-gradient step of MoE training,
+ * which contracts over each expert's tokens (page "DeepSeek开源周第三天DeepGEMM",
+ * section "DeepGEMM提供三种FP8GEMM实现", names the grouped kinds by the training
+ * forward pass and inference; this is the same scaled product with the K range
+ * restricted per group, the reading this library takes for the backward step).
+ *
+ *   D[g][m][n] = sum over the K blocks kb of segment g of
+ *                sA[m,kb] * sB[n/128,kb] * sum_{k in kb} A[m,k] * B[n,k]
+ *
+ *   A   [M][K] FP8 (K-major: the token axis contiguous), shared by all groups
+ *   B   [N][K] FP8 (K-major), shared by all groups
+ *   sA  MN-major [ceil(K/128)][ld_sA] floats, ld_sA >= M, ld_sA % 4 == 0
+ *   sB  [ceil(N/128)][ceil(K/128)] floats
+ *   k_sizes [G] int32 on the device: group g covers K columns
+ *       [k_sizes[0] + ... + k_sizes[g-1], ... + k_sizes[g]); every length a
+ *       multiple of 128 (K blocks never straddle groups), their sum <= K.
+ *       The host never reads them (graph-capturable); a length that is
+ *       negative or not a multiple of 128, or a sum past K, is recorded as
+ *       FG_ERR_DEVICE_CHECK (detail: the group, or G for the sum) and the
+ *       walk rounds it down / clips it to K.
+ *   D   [G][M][N] bfloat16 (the _f32out form: float), 16-byte aligned; every
+ *       element is written (an empty segment gives zeros).
+ * K % 16 == 0, N % 8 == 0; M == 0 is a no-op. */
+fg_status fg_k_grouped_gemm_fp8_nt(const void *A, int a_fmt, const float *sA, int ld_sA,
+                                   const void *B, int b_fmt, const float *sB, void *D,
+                                   const int32_t *k_sizes, int G, int M, int N, int K, void *stream);
+fg_status fg_k_grouped_gemm_fp8_nt_f32out(const void *A, int a_fmt, const float *sA, int ld_sA,
+                                          const void *B, int b_fmt, const float *sB, float *D,
+                                          const int32_t *k_sizes, int G, int M, int N, int K,
+                                          void *stream);
+
 /* Layout helper (the page's "LHS scales must be TMA-aligned and transposed",
  * section "基本用法"): src is row-major [batches][rows][kb], dst receives
  * [batches][kb][ld_dst] with ld_dst >= rows, ld_dst % 4 == 0; padding entries

@@ -43,6 +43,8 @@ SIGNATURES = {
     "fg_gemm_fp8_nt_f32out": (_I, [_P, _I, _P, _I, _P, _I, _P, _P, _I, _I, _I, _P]),
     "fg_grouped_gemm_fp8_contiguous_f32out": (_I, [_P, _I, _P, _I, _P, _I, _P, _P, _P, _I, _I, _I, _I, _P]),
     "fg_grouped_gemm_fp8_masked_f32out": (_I, [_P, _I, _P, _I, _P, _I, _P, _P, _P, _I, _I, _I, _I, _P]),
+    "fg_k_grouped_gemm_fp8_nt": (_I, [_P, _I, _P, _I, _P, _I, _P, _P, _P, _I, _I, _I, _I, _P]),
+    "fg_k_grouped_gemm_fp8_nt_f32out": (_I, [_P, _I, _P, _I, _P, _I, _P, _P, _P, _I, _I, _I, _I, _P]),
     "fg_scales_a_to_mn_major": (_I, [_P, _P, _I, _I, _I, _I, _P]),
     "fg_scales_a_ld": (_I, [_I]),
     "fg_quantize_fp8_per_token": (_I, [_P, _I, _I, _P, _P, _I, _P, _I, _I, _I, _P]),
@@ -240,6 +242,35 @@ def _masked(name, d_dtypes, A, sA, B, sB, D, masked_m, a_fmt, b_fmt, stream):
     _launch(name, (("A", A), ("sA", sA), ("B", B), ("sB", sB), ("D", D), ("masked_m", masked_m)), stream,
             A.data_ptr(), _fmt_of(A, a_fmt), sA.data_ptr(), sA.shape[2], B.data_ptr(), _fmt_of(B, b_fmt),
             sB.data_ptr(), D.data_ptr(), masked_m.data_ptr(), G, M_cap, n, k)
+    return D
+
+
+def fg_k_grouped_gemm_fp8_nt(A, sA, B, sB, D, k_sizes, *, a_fmt=None, b_fmt=None, stream=None):
+    """K-grouped layout: D[g] = A[:, seg_g] . B[:, seg_g]^T with the fine-grained
+    scales, one 128-aligned K segment per group (k_sizes [G] int32 on the device).
+    A [M, K], sA MN-major [ceil(K/128), ld], B [N, K], sB [ceil(N/128), ceil(K/128)],
+    D [G, M, N] bfloat16."""
+    return _k_grouped("fg_k_grouped_gemm_fp8_nt", _BF16, A, sA, B, sB, D, k_sizes, a_fmt, b_fmt, stream)
+
+
+def fg_k_grouped_gemm_fp8_nt_f32out(A, sA, B, sB, D, k_sizes, *, a_fmt=None, b_fmt=None, stream=None):
+    """fg_k_grouped_gemm_fp8_nt with an FP32 D [G, M, N]."""
+    return _k_grouped("fg_k_grouped_gemm_fp8_nt_f32out", _F32, A, sA, B, sB, D, k_sizes, a_fmt, b_fmt, stream)
+
+
+def _k_grouped(name, d_dtypes, A, sA, B, sB, D, k_sizes, a_fmt, b_fmt, stream):
+    _need(A, "A", _FP8, 2), _need(B, "B", _FP8, 2), _need(sA, "sA", _F32, 2)
+    _need(sB, "sB", _F32, 2), _need(D, "D", d_dtypes, 3), _need(k_sizes, "k_sizes", _I32, 1)
+    M, K = A.shape
+    N = B.shape[0]
+    G = k_sizes.shape[0]
+    if B.shape[1] != K or tuple(D.shape) != (G, M, N):
+        raise ValueError(f"shape mismatch A{tuple(A.shape)} B{tuple(B.shape)} D{tuple(D.shape)} G={G}")
+    if sA.shape[0] != _cdiv(K, 128) or tuple(sB.shape) != (_cdiv(N, 128), _cdiv(K, 128)):
+        raise ValueError("scale shapes do not fit")
+    _launch(name, (("A", A), ("sA", sA), ("B", B), ("sB", sB), ("D", D), ("k_sizes", k_sizes)), stream,
+            A.data_ptr(), _fmt_of(A, a_fmt), sA.data_ptr(), sA.shape[1], B.data_ptr(), _fmt_of(B, b_fmt),
+            sB.data_ptr(), D.data_ptr(), k_sizes.data_ptr(), G, M, N, K)
     return D
 
 

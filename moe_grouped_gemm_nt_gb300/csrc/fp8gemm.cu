@@ -417,6 +417,72 @@ fg_status run(const void *A, int a_fmt, const float *sA, int ld_sA, const void *
     return Kernel<256, 4, KIND, false, F32OUT>::launch(ta, tb, td, tsa, p, grid, 1, stream);
 }
 
+// K-grouped entry points: G groups, each an NT product over its own segment of
+// K (segment lengths on the device), all sharing A [M][K] and B [N][K]; output
+// planes D [G][M][N].  Persistent one-CTA tiles (128 x 256, or 128 x 128 when
+// the 256-wide tiles would leave SMs idle), no split-K.
+template <bool F32OUT>
+fg_status run_kgrouped(const void *A, int a_fmt, const float *sA, int ld_sA, const void *B, int b_fmt,
+                       const float *sB, void *D, const int32_t *k_sizes, int G, int M, int N, int K,
+                       cudaStream_t stream) {
+    if (!A || !B || !sA || !sB || !D || !k_sizes) return FG_ERR_INVALID_ARG;
+    if (!fmt_ok(a_fmt) || !fmt_ok(b_fmt)) return FG_ERR_INVALID_ARG;
+    if (M < 0 || N < 1 || K < 1 || G < 1 || ld_sA < M || ld_sA < 1) return FG_ERR_INVALID_ARG;
+    if (K % 16 != 0 || N % 8 != 0) return FG_ERR_UNSUPPORTED;
+    if (ld_sA % 4 != 0) return FG_ERR_MISALIGNED;
+    if (!aligned16(A) || !aligned16(B) || !aligned16(D) || !aligned16(sA) || !aligned4(sB)) return FG_ERR_MISALIGNED;
+    const long long tiles256 = (long long)G * cdiv(M, fg::BLOCK_M) * cdiv(N, 256);
+    if ((long long)G * M > INT32_MAX || tiles256 * 2 > INT32_MAX || G > 65535) return FG_ERR_UNSUPPORTED;
+    if (M == 0) return FG_OK;
+
+    DeviceInfo *dev = nullptr;
+    if (fg_status st = device_info(&dev); st != FG_OK) return st;
+    int sms = dev->num_sms;
+    const int ovr = g_num_sms_override.load();
+    if (ovr > 0 && ovr < sms) sms = ovr;
+    // 256-wide tiles unless they fill less than three quarters of the SMs
+    // four times over and 128-wide ones have more tiles (or the width is forced)
+    int BN = 256;
+    if (g_force_bn.load() == 128 || (g_force_bn.load() == 0 && tiles256 * 4 < (long long)sms * 3)) BN = 128;
+
+    const int num_kb = cdiv(K, fg::BLOCK_K);
+    CUtensorMap ta, tb, td, tsa;
+    const uint64_t ddims[3] = {(uint64_t)N, (uint64_t)M, (uint64_t)G};
+    const uint64_t dstrides[2] = {(uint64_t)N * (F32OUT ? 4 : 2), (uint64_t)N * (F32OUT ? 4 : 2) * (uint64_t)M};
+    const uint32_t dbox[3] = {F32OUT ? 32u : 64u, 32u, 1u};
+    if (!encode_scales_a(&tsa, sA, ld_sA, M, num_kb, 1, false) ||
+        !encode_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, (uint64_t)K, (uint64_t)M, (uint64_t)K, fg::BLOCK_K,
+                   fg::BLOCK_M) ||
+        !encode_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, (uint64_t)K, (uint64_t)N, (uint64_t)K, fg::BLOCK_K,
+                   (uint32_t)BN) ||
+        !encode(&td, F32OUT ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, D, 3, ddims,
+                dstrides, dbox, CU_TENSOR_MAP_SWIZZLE_128B))
+        return cuda_fail();
+
+    GemmParams p{};
+    p.rows = M;
+    p.n = N;
+    p.k = K;
+    p.num_groups = G;
+    p.num_kb = num_kb;
+    p.num_nb = cdiv(N, 128);
+    p.num_n_blocks = cdiv(N, BN);
+    p.num_m_blocks = cdiv(M, fg::BLOCK_M);
+    p.group_m = raster_group_m(fg::KIND_KGROUPED, p.num_m_blocks, K);
+    p.idesc = fg::make_idesc_f8f6f4(fg::BLOCK_M, BN, (uint32_t)a_fmt, (uint32_t)b_fmt);
+    p.sB = sB;
+    p.k_sizes = k_sizes;
+    p.D = D;
+    p.status = dev->status;
+    p.timeout_ns = (unsigned long long)g_watchdog_ms.load() * 1000000ull;
+    p.debug_skip_iter = g_debug_skip_iter.exchange(-1);
+    const long long tiles = (long long)G * p.num_m_blocks * p.num_n_blocks;
+    const int grid = (int)(tiles < sms ? tiles : sms);
+    if (BN == 128)
+        return Kernel<128, 6, fg::KIND_KGROUPED, false, F32OUT>::launch(ta, tb, td, tsa, p, grid, 1, stream);
+    return Kernel<256, 4, fg::KIND_KGROUPED, false, F32OUT>::launch(ta, tb, td, tsa, p, grid, 1, stream);
+}
+
 }  // namespace
 
 namespace {
@@ -484,6 +550,20 @@ fg_status fg_grouped_gemm_fp8_masked_f32out(const void *A, int a_fmt, const floa
                                             int M_cap, int n, int k, void *stream) {
     return run<fg::KIND_MASKED, true>(A, a_fmt, sA, ld_sA, B, b_fmt, sB, D, nullptr, masked_m, M_cap, G, n, k,
                                       static_cast<cudaStream_t>(stream));
+}
+
+fg_status fg_k_grouped_gemm_fp8_nt(const void *A, int a_fmt, const float *sA, int ld_sA, const void *B, int b_fmt,
+                                   const float *sB, void *D, const int32_t *k_sizes, int G, int M, int N, int K,
+                                   void *stream) {
+    return run_kgrouped<false>(A, a_fmt, sA, ld_sA, B, b_fmt, sB, D, k_sizes, G, M, N, K,
+                               static_cast<cudaStream_t>(stream));
+}
+
+fg_status fg_k_grouped_gemm_fp8_nt_f32out(const void *A, int a_fmt, const float *sA, int ld_sA, const void *B,
+                                          int b_fmt, const float *sB, float *D, const int32_t *k_sizes, int G,
+                                          int M, int N, int K, void *stream) {
+    return run_kgrouped<true>(A, a_fmt, sA, ld_sA, B, b_fmt, sB, D, k_sizes, G, M, N, K,
+                              static_cast<cudaStream_t>(stream));
 }
 
 fg_status fg_scales_a_to_mn_major(const float *src, float *dst, int batches, int rows, int kb, int ld_dst,

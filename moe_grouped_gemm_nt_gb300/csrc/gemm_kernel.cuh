@@ -58,7 +58,7 @@
 
 namespace fg {
 
-enum : int { KIND_DENSE = 0, KIND_CONTIGUOUS = 1, KIND_MASKED = 2 };
+enum : int { KIND_DENSE = 0, KIND_CONTIGUOUS = 1, KIND_MASKED = 2, KIND_KGROUPED = 3 };
 
 // device-side status codes (same values as fg_status in fp8gemm.h)
 enum : uint32_t { DEV_ERR_TIMEOUT = 5, DEV_ERR_CHECK = 6 };
@@ -92,7 +92,9 @@ struct GemmParams {
     const float *sB;
     const int32_t *m_indices;
     const int32_t *masked_m;
+    const int32_t *k_sizes;  // K-grouped layout: [G] K-segment lengths (multiples of 128)
     void *D;           // bfloat16 [rows][n], or float [rows][n] for the FP32-output instantiations
+                       // (K-grouped: [G][rows][n])
     uint32_t *status;  // [0] first error code, [1] its detail
     unsigned long long timeout_ns;
     int debug_skip_iter;  // producer leaves this K iteration unarmed (-1: never)
@@ -133,7 +135,21 @@ struct Tile {
     int a_row;      // first row of the tile in the 2-D row space of A and D
     int b_row;      // first row of the tile in the 2-D row space of B ([G*n][k])
     int row_limit;  // rows of the tile below the bound (dense m, masked count)
+    int kb_lo, kb_hi;  // K-grouped layout: the tile's K blocks (its group's segment)
 };
+
+// K-grouped layout: position of the scan over the segment lengths (group g
+// starts at K block kb).  Every role walks its tiles in increasing order, and
+// the tiles of one group are consecutive, so the scan only moves forward.
+struct KScan {
+    int g = 0;
+    int kb = 0;
+};
+
+__device__ __forceinline__ int k_segment_blocks(const GemmParams &p, int g) {
+    const int s = __ldg(p.k_sizes + g);
+    return s > 0 ? s / BLOCK_K : 0;
+}
 
 // M blocks of the whole walk (masked: the valid blocks of all groups).
 template <int KIND>
@@ -153,9 +169,23 @@ __device__ __forceinline__ int total_m_blocks(const GemmParams &p) {
 // N blocks with M varying fastest, so the CTAs running at the same time share
 // the group's A rows (kept in L2) while B streams through once per group.
 // group_m = 1 makes N vary fastest (B kept in L2, A streamed once).
+// K-grouped layout: the tiles of group g (all M x N blocks of its output) come
+// before those of group g + 1, each group walked like a dense problem.
 template <int BN, int KIND>
-__device__ __forceinline__ Tile get_tile(const GemmParams &p, int t, int mblocks) {
+__device__ __forceinline__ Tile get_tile(const GemmParams &p, int t, int mblocks, KScan &scan) {
     Tile ti;
+    ti.kb_lo = 0;
+    ti.kb_hi = p.num_kb;
+    if constexpr (KIND == KIND_KGROUPED) {
+        const int per_g = mblocks * p.num_n_blocks;
+        const int g = t / per_g;
+        t -= g * per_g;
+        if (g < scan.g) scan = KScan{};
+        while (scan.g < g) scan.kb += k_segment_blocks(p, scan.g++);
+        ti.kb_lo = min(scan.kb, p.num_kb);
+        ti.kb_hi = min(scan.kb + k_segment_blocks(p, g), p.num_kb);
+        ti.group = g;
+    }
     const int per_group = p.group_m * p.num_n_blocks;
     const int grp = t / per_group;
     const int rem = t - grp * per_group;
@@ -163,9 +193,11 @@ __device__ __forceinline__ Tile get_tile(const GemmParams &p, int t, int mblocks
     const int gm = min(p.group_m, mblocks - m0);
     const int mb_lin = m0 + rem % gm;
     ti.n_blk = rem / gm;
-    if constexpr (KIND == KIND_DENSE) {
+    if constexpr (KIND == KIND_DENSE || KIND == KIND_KGROUPED) {
+        // (K-grouped: A and B are shared by the groups; the group selects the
+        // K range and the output plane)
         ti.valid = 1;
-        ti.group = 0;
+        if constexpr (KIND == KIND_DENSE) ti.group = 0;
         ti.m_blk = mb_lin;
         ti.a_row = mb_lin * BLOCK_M;
         ti.b_row = ti.n_blk * BN;
@@ -349,9 +381,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
         }
     }
+    if constexpr (KIND == KIND_KGROUPED) {
+        // segment lengths must be multiples of 128 and fit in K; others are
+        // reported (the walk rounds them down and clips them to K)
+        if (blockIdx.x == 0 && warp == 0 && lane == 0) {
+            long long total = 0;
+            for (int g = 0; g < p.num_groups; ++g) {
+                const int c = __ldg(p.k_sizes + g);
+                if (c < 0 || c % BLOCK_K != 0) record_error(p, DEV_ERR_CHECK, (uint32_t)g);
+                total += c > 0 ? c : 0;
+            }
+            if (total > p.k) record_error(p, DEV_ERR_CHECK, (uint32_t)p.num_groups);
+        }
+    }
 
     const int m_blocks = total_m_blocks<KIND>(p);
-    const int num_tiles = m_blocks * p.num_n_blocks;
+    const int num_tiles = m_blocks * p.num_n_blocks * (KIND == KIND_KGROUPED ? p.num_groups : 1);
     // This CTA's work: persistent tiles t_begin, t_begin + t_step, ... over all
     // K blocks, or (split-K) the one tile of its cluster over its K range.
     int t_begin = blockIdx.x, t_step = gridDim.x, kb_begin = 0, kb_end = p.num_kb;
@@ -370,15 +415,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (lane == 0) {
             uint32_t it = 0;
             bool ok = true;
+            KScan scan;
             for (int t = t_begin; t < num_tiles && ok; t += t_step) {
-                const Tile ti = get_tile<BN, KIND>(p, t, m_blocks);
+                const Tile ti = get_tile<BN, KIND>(p, t, m_blocks, scan);
                 if (!ti.valid) continue;
                 // RHS block scales of the two column halves of this tile
                 const int nb0 = min((ti.n_blk * BN) / 128, p.num_nb - 1);
                 const int nb1 = min((ti.n_blk * BN + BN / 2) / 128, p.num_nb - 1);
-                const float *sb0 = p.sB + ((size_t)ti.group * p.num_nb + nb0) * p.num_kb;
-                const float *sb1 = p.sB + ((size_t)ti.group * p.num_nb + nb1) * p.num_kb;
-                for (int kb = kb_begin; kb < kb_end; ++kb, ++it) {
+                const int bgroup = KIND == KIND_KGROUPED ? 0 : ti.group;  // K-grouped: one B for all groups
+                const float *sb0 = p.sB + ((size_t)bgroup * p.num_nb + nb0) * p.num_kb;
+                const float *sb1 = p.sB + ((size_t)bgroup * p.num_nb + nb1) * p.num_kb;
+                const int kb_stop = KIND == KIND_KGROUPED ? ti.kb_hi : kb_end;
+                for (int kb = KIND == KIND_KGROUPED ? ti.kb_lo : kb_begin; kb < kb_stop; ++kb, ++it) {
                     const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
                     const uint32_t q = it % SCALE_STAGES, qph = (it / SCALE_STAGES) & 1u;
                     if (!wait_phase(empty_bar(s), ph ^ 1u, abort_flag, p, ROLE_PRODUCER) ||
@@ -423,10 +471,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (lane == 0) {
             uint32_t it = 0;
             bool ok = true;
+            KScan scan;
             for (int t = t_begin; t < num_tiles && ok; t += t_step) {
-                const Tile ti = get_tile<BN, KIND>(p, t, m_blocks);
+                const Tile ti = get_tile<BN, KIND>(p, t, m_blocks, scan);
                 if (!ti.valid) continue;
-                for (int kb = kb_begin; kb < kb_end; ++kb, ++it) {
+                const int kb_stop = KIND == KIND_KGROUPED ? ti.kb_hi : kb_end;
+                for (int kb = KIND == KIND_KGROUPED ? ti.kb_lo : kb_begin; kb < kb_stop; ++kb, ++it) {
                     const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
                     const uint32_t b = it & (NTB - 1u), bph = (it / NTB) & 1u;
                     if (!wait_phase(tempty_bar(b), bph ^ 1u, abort_flag, p, ROLE_MMA) ||
@@ -468,8 +518,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // scale-ring entry q (phase qph) of the current K iteration
         uint32_t b = 0, bph = 0, q = 0, qph = 0;
         bool ok = true;
+        KScan scan;
         for (int t = t_begin; t < num_tiles && ok; t += t_step) {
-            const Tile ti = get_tile<BN, KIND>(p, t, m_blocks);
+            const Tile ti = get_tile<BN, KIND>(p, t, m_blocks, scan);
             if (!ti.valid) {
                 if constexpr (KIND == KIND_CONTIGUOUS) {
                     // a skipped block must be all padding (-1 rows); a group id
@@ -502,7 +553,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
             for (int j = 0; j < COLS / 2; ++j) acc2[j] = 0ull;
 
-            for (int kb = kb_begin; kb < kb_end; ++kb) {
+            // (K-grouped: an empty segment leaves the sums at zero, and zeros are stored)
+            const int kb_stop = KIND == KIND_KGROUPED ? ti.kb_hi : kb_end;
+            for (int kb = KIND == KIND_KGROUPED ? ti.kb_lo : kb_begin; kb < kb_stop; ++kb) {
                 const bool got = wait_phase(sfull_bar(q), qph, abort_flag, p, ROLE_EPILOGUE) &&
                                  wait_phase(tfull_bar(b), bph, abort_flag, p, ROLE_EPILOGUE);
                 if (!__all_sync(0xffffffffu, got)) {
@@ -566,14 +619,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             float acc[COLS];
 #pragma unroll
             for (int j = 0; j < COLS / 2; ++j) unpack_f32x2(acc2[j], acc[2 * j], acc[2 * j + 1]);
-            const int d_row = ti.a_row + sub * 32;  // first row of this warp's block in D
+            // first row of this warp's block in D (K-grouped: within the group's
+            // output plane, the third coordinate of D's tensor map)
+            const int d_row = ti.a_row + sub * 32;
+            constexpr bool CLIPPED = KIND == KIND_DENSE || KIND == KIND_KGROUPED;
             bool use_tma;
-            if constexpr (KIND == KIND_DENSE)
+            if constexpr (CLIPPED)
                 use_tma = true;  // rows past m are clipped by the tensor map bounds
             else
                 use_tma = __all_sync(0xffffffffu, row_ok);
             if (use_tma) {
-                const bool rows_in = (KIND != KIND_DENSE) || (sub * 32 < ti.row_limit);
+                const bool rows_in = !CLIPPED || (sub * 32 < ti.row_limit);
                 if constexpr (F32OUT) {
                     // FP32 boxes: 32 rows x 32 columns (128 bytes per row, same swizzle)
 #pragma unroll
@@ -592,7 +648,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         fence_proxy_async_smem();
                         __syncwarp();
                         if (lane == 0) {
-                            tma_store_2d(&tmap_d, stg, x, d_row);
+                            if constexpr (KIND == KIND_KGROUPED)
+                                tma_store_3d(&tmap_d, stg, x, d_row, ti.group);
+                            else
+                                tma_store_2d(&tmap_d, stg, x, d_row);
                             bulk_commit_group();
                         }
                     }
@@ -613,7 +672,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) {
-                        tma_store_2d(&tmap_d, stg, x, d_row);
+                        if constexpr (KIND == KIND_KGROUPED)
+                            tma_store_3d(&tmap_d, stg, x, d_row, ti.group);
+                        else
+                            tma_store_2d(&tmap_d, stg, x, d_row);
                         bulk_commit_group();
                     }
                 }
@@ -661,7 +723,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 any_abort |= ld_shared_cluster_u32(map_shared_rank(smem_u32((const void *)abort_flag), q)) != 0u;
             const bool tile_ok = t_begin < num_tiles && !any_abort;
             if (tile_ok && warp < NUM_EPI_WARPS) {
-                const Tile ti = get_tile<BN, KIND>(p, t_begin, m_blocks);
+                KScan scan;
+                const Tile ti = get_tile<BN, KIND>(p, t_begin, m_blocks, scan);
                 if (ti.valid) {
                     constexpr int CH = BN / 4;  // 16-byte chunks per partial row
                     constexpr int MAX_SPLIT = 8;

@@ -185,3 +185,23 @@ def test_binding_rejects_operands_on_different_devices():
         fg._common_device((("A", t0), ("D", t0)), stream=SimpleNamespace(device=d1))
     # a raw stream handle cannot be checked and is accepted as given
     assert fg._common_device((("A", t0),), stream=12345) == d0
+
+
+def test_k_grouped_argument_checks():
+    """The K-grouped calls check their arguments on the host (no launch)."""
+    L = fg.lib()
+    ok = dict(A=FAKE, a_fmt=0, sA=FAKE, ld=128, B=FAKE, b_fmt=0, sB=FAKE, D=FAKE, ks=FAKE, G=2, M=128, N=256,
+              K=512)
+
+    def call(f32=False, **kw):
+        a = dict(ok, **kw)
+        f = L.fg_k_grouped_gemm_fp8_nt_f32out if f32 else L.fg_k_grouped_gemm_fp8_nt
+        return f(a["A"], a["a_fmt"], a["sA"], a["ld"], a["B"], a["b_fmt"], a["sB"], a["D"], a["ks"], a["G"],
+                 a["M"], a["N"], a["K"], None)
+
+    for f32 in (False, True):
+        assert call(f32, ks=None) == 1 and call(f32, A=None) == 1 and call(f32, G=0) == 1
+        assert call(f32, b_fmt=5) == 1 and call(f32, ld=64) == 1 and call(f32, N=0) == 1
+        assert call(f32, K=520) == 3 and call(f32, N=260) == 3
+        assert call(f32, ld=132 + 2) == 2 and call(f32, D=FAKE + 4) == 2
+        assert call(f32, M=0) == 0  # nothing to do: no launch

@@ -351,3 +351,24 @@ def bf16_bits(x: np.ndarray) -> np.ndarray:
     u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
     assert not np.any(u & 0xFFFF), "values are not bfloat16"
     return (u >> 16).astype(np.uint16)
+
+
+# K-grouped layout (the weight gradient of the contiguous workload): for each
+# (n, k) weight shape, G experts of 8192 tokens; the gradient of B[g] [n][k]
+# contracts the output gradient [tokens][n] with the activations [tokens][k]
+# over the group's tokens, i.e. M = n, N = k, one 8192-long K segment per group.
+KGROUPED_G = [4, 8]
+KGROUPED_TOKENS_PER_GROUP = CONTIGUOUS_ROWS_PER_GROUP
+
+
+def k_grouped_shapes():
+    """(G, M, N, tokens per group) of the K-grouped workload."""
+    return [(G, n, k, KGROUPED_TOKENS_PER_GROUP) for G in KGROUPED_G for (n, k) in GROUPED_NK]
+
+
+def k_grouped(M, N, k_sizes, seed, b_fmt=E4M3, K=None) -> Dense:
+    """Operands of a K-grouped problem: A [M][K], B [N][K] with the NT GEMM's
+    scaling (1 x 128 LHS groups, 128 x 128 RHS blocks), K = sum of the segment
+    lengths unless given.  Returns a Dense holding them (m = M, n = N, k = K)."""
+    total = int(np.sum(k_sizes))
+    return dense(M, N, total if K is None else K, seed, b_fmt=b_fmt)
