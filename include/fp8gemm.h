@@ -239,6 +239,30 @@ fg_status fg_query_dense_plan_ex(int m, int n, int k, int *block_n, int *split_k
  * summation order; FG_ERR_INVALID_ARG for other values. */
 fg_status fg_set_pair_mode(int mode);
 
+/* Swapped operand roles ("swap-AB") for later calls: the weights (B) take the
+ * tensor core's 128-row role and the rows of A (tokens, at most 256 per tile)
+ * its N role, so a group with few rows multiplies, loads and promotes no empty
+ * rows, and a masked call launches tiles only over the weights of the groups
+ * that have rows.  The output, the scales and every other contract are those
+ * of the unswapped call; each element still receives sum_kb (sA * sB) * P.
+ * Applies to dense calls with m <= 256 and masked calls with M_cap <= 256.
+ * -1 (default, automatic) and 0: never -- measured slower than the unswapped
+ * plans on every problem of the dense sweep with m <= 128 and of the masked
+ * workloads (a swapped tile covers 128 weight rows, so A is read once per 128
+ * weights instead of once per 256); 1: wherever it applies (a forced split_k
+ * then sets its split-K cluster size).  The pages' design has no counterpart
+ * (their small-M path keeps the operand roles).  Results differ from the
+ * unswapped path only by FP32 summation order. */
+fg_status fg_set_swap_mode(int mode);
+
+/* The tile plan a call of this layout and shape would use on the current
+ * device.  kind: 0 dense (rows = m, G = 1), 1 contiguous (rows = M), 2 masked
+ * (rows = M_cap).  plan[4] receives: [0] the tile width (output columns per
+ * tile; with swapped roles, rows of A per tile), [1] the split-K cluster size
+ * (1 = none), [2] 1 for CTA-pair tiles, [3] 1 for swapped operand roles.
+ * Host-only (reads device attributes, launches nothing). */
+fg_status fg_query_plan(int kind, int rows, int G, int n, int k, int *plan);
+
 /* Programmatic dependent launch of the GEMM kernels (default on): a call's
  * CTAs may start while the previous kernel of the stream finishes, set up
  * their shared memory, tensor memory and barriers, and wait for the previous

@@ -56,6 +56,8 @@ SIGNATURES = {
     "fg_query_dense_plan": (_I, [_I, _I, _I, ctypes.POINTER(_I), ctypes.POINTER(_I)]),
     "fg_query_dense_plan_ex": (_I, [_I, _I, _I, ctypes.POINTER(_I), ctypes.POINTER(_I), ctypes.POINTER(_I)]),
     "fg_set_pair_mode": (_I, [_I]),
+    "fg_set_swap_mode": (_I, [_I]),
+    "fg_query_plan": (_I, [_I, _I, _I, _I, _I, ctypes.POINTER(_I)]),
     "fg_status_string": (ctypes.c_char_p, [_I]),
     "fg_version": (_I, []),
     "fg_debug_skip_producer_iteration": (_I, [_I]),
@@ -380,6 +382,18 @@ def fg_query_dense_plan_ex(m: int, n: int, k: int):
 def fg_set_pair_mode(mode: int) -> None:
     """-1: CTA-pair tiles where they apply (default); 0: never; 1: every persistent 256-wide plan."""
     _check("fg_set_pair_mode", lib().fg_set_pair_mode(int(mode)))
+
+
+def fg_set_swap_mode(mode: int) -> None:
+    """-1: swapped operand roles where they apply (default: masked, M_cap <= 256); 0: never; 1: wherever allowed."""
+    _check("fg_set_swap_mode", lib().fg_set_swap_mode(int(mode)))
+
+
+def fg_query_plan(kind: int, rows: int, G: int, n: int, k: int):
+    """(tile width, split_k, cta_pair, swap_ab) of a call: kind 0 dense, 1 contiguous, 2 masked."""
+    pl = (ctypes.c_int * 4)()
+    _check("fg_query_plan", lib().fg_query_plan(int(kind), int(rows), int(G), int(n), int(k), pl))
+    return tuple(pl)
 
 
 def fg_set_programmatic_launch(enable: bool) -> None:

@@ -2,7 +2,8 @@
 
 The library is a plain C ABI shared object (include/fp8gemm.h); the CUDA
 runtime is linked statically, so loading it needs no GPU driver, and the
-driver's tensor-map encoder is resolved at run time.
+driver's tensor-map encoder is resolved at run time.  The translation units
+compile in parallel (one nvcc process each) and are linked into one object.
 """
 from __future__ import annotations
 
@@ -14,9 +15,11 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(BUILD_DIR, "libfp8gemm.so")
-SOURCES = ["fp8gemm.cu"]
-HEADERS = ["gemm_kernel.cuh", "gemm_pair_kernel.cuh", "quantize_kernel.cuh", "ptx.cuh"]
+SOURCES = ["fp8gemm.cu", "swap.cu"]
+HEADERS = ["gemm_kernel.cuh", "gemm_pair_kernel.cuh", "gemm_swap_kernel.cuh", "quantize_kernel.cuh", "ptx.cuh",
+           "host_common.cuh", "swap.h"]
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
+COMMON_FLAGS = ["-std=c++17", "-O3", "-lineinfo", *ARCH_FLAGS, "-Xcompiler", "-fPIC"]
 
 
 def nvcc() -> str:
@@ -40,14 +43,26 @@ def build(force: bool = False, verbose: bool = False) -> str:
     if not force and not _stale():
         return LIB_PATH
     os.makedirs(BUILD_DIR, exist_ok=True)
-    tmp = LIB_PATH + f".tmp{os.getpid()}"
-    cmd = [nvcc(), "-std=c++17", "-O3", "-lineinfo", *ARCH_FLAGS, "-shared", "-Xcompiler", "-fPIC",
-           "-cudart", "static", "-I", os.path.join(ROOT, "include"),
-           *[os.path.join(CSRC, s) for s in SOURCES], "-o", tmp]
-    if verbose:
-        cmd.insert(1, "-Xptxas=-v")
-    subprocess.run(cmd, check=True)
-    os.replace(tmp, LIB_PATH)
+    tag = f"tmp{os.getpid()}"
+    objs, procs = [], []
+    for src in SOURCES:
+        obj = os.path.join(BUILD_DIR, f"{os.path.splitext(src)[0]}.{tag}.o")
+        cmd = [nvcc(), *COMMON_FLAGS, "-I", os.path.join(ROOT, "include"), "-c", os.path.join(CSRC, src), "-o", obj]
+        if verbose:
+            cmd.insert(1, "-Xptxas=-v")
+        procs.append(subprocess.Popen(cmd))
+        objs.append(obj)
+    failed = [p.args for p in procs if p.wait() != 0]
+    try:
+        if failed:
+            raise subprocess.CalledProcessError(1, failed[0])
+        tmp = LIB_PATH + f".{tag}"
+        subprocess.run([nvcc(), *ARCH_FLAGS, "-shared", "-cudart", "static", *objs, "-o", tmp], check=True)
+        os.replace(tmp, LIB_PATH)
+    finally:
+        for o in objs:
+            if os.path.exists(o):
+                os.remove(o)
     return LIB_PATH
 
 

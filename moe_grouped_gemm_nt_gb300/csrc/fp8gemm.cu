@@ -1,27 +1,27 @@
 // fp8gemm.cu -- C ABI of the FP8 NT GEMM library (declared in include/fp8gemm.h):
 // argument checks, TMA tensor-map encoding, kernel selection and launch, and the
 // per-device status word written by the kernels' watchdogs and range checks.
-#include <cuda.h>
-#include <cuda_runtime.h>
-#include <cudaTypedefs.h>
-
-#include <algorithm>
-#include <atomic>
-#include <cstdint>
-#include <cstdlib>
-#include <mutex>
-
-#include "../../include/fp8gemm.h"
-#include "gemm_kernel.cuh"
+#include "host_common.cuh"
 #include "gemm_pair_kernel.cuh"
 #include "quantize_kernel.cuh"
+#include "swap.h"
 
-namespace {
+namespace fg {
 
-using fg::GemmParams;
+// Row-major [batches][rows][kb] -> MN-major [batches][kb][ld] (zero padding).
+__global__ void scales_to_mn_major_kernel(const float *__restrict__ src, float *__restrict__ dst, int rows,
+                                          int kb, int ld) {
+    const int r = blockIdx.x * blockDim.x + threadIdx.x;
+    const int j = blockIdx.y;
+    const size_t b = blockIdx.z;
+    if (r >= ld) return;
+    const float v = r < rows ? src[(b * rows + r) * kb + j] : 0.f;
+    dst[(b * kb + j) * ld + r] = v;
+}
 
-constexpr int kMaxDevices = 64;
-constexpr uint32_t kDefaultWatchdogMs = 2000;
+}  // namespace fg
+
+namespace fgh {
 
 // [0] first error code, [1] detail; one copy per device (module globals are per context)
 __device__ uint32_t g_status[2];
@@ -29,19 +29,14 @@ __device__ uint32_t g_status[2];
 std::atomic<int> g_num_sms_override{0};
 std::atomic<uint32_t> g_watchdog_ms{kDefaultWatchdogMs};
 std::atomic<int> g_debug_skip_iter{-1};
+std::atomic<int> g_force_bn{0};
+std::atomic<int> g_pdl{1};
+std::atomic<int> g_force_split{0};
+std::atomic<int> g_pair_mode{-1};
+std::atomic<int> g_swap_mode{-1};
 
-// Per-device facts read once.  `ready` is published with release after the
-// other fields are written, and read with acquire, so a thread that sees it
-// set also sees the status address and the SM count.
-struct DeviceInfo {
-    std::atomic<int> ready{0};
-    int num_sms = 0;
-    uint32_t *status = nullptr;
-};
 DeviceInfo g_dev[kMaxDevices];
 std::mutex g_dev_mutex;
-
-fg_status cuda_fail() { return FG_ERR_CUDA; }
 
 fg_status device_info(DeviceInfo **out) {
     int dev = 0;
@@ -63,138 +58,11 @@ fg_status device_info(DeviceInfo **out) {
     return FG_OK;
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void *p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    });
-    return fn;
-}
+}  // namespace fgh
 
-// Tiled tensor map (rank 2 or 3) over a row-major array: dims[0] innermost,
-// strides[i] = bytes between consecutive indices of dimension i+1.
-bool encode(CUtensorMap *map, CUtensorMapDataType dt, const void *base, int rank, const uint64_t *dims,
-            const uint64_t *strides, const uint32_t *box, CUtensorMapSwizzle swizzle) {
-    auto fn = encode_fn();
-    if (!fn) return false;
-    cuuint64_t d[3], st[2];
-    cuuint32_t bx[3], es[3] = {1, 1, 1};
-    for (int i = 0; i < rank; ++i) {
-        d[i] = dims[i];
-        bx[i] = box[i];
-    }
-    for (int i = 0; i + 1 < rank; ++i) st[i] = strides[i];
-    CUresult r = fn(map, dt, (cuuint32_t)rank, const_cast<void *>(base), d, st, bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                    swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS;
-}
+namespace {
 
-bool encode_2d(CUtensorMap *map, CUtensorMapDataType dt, const void *base, uint64_t inner, uint64_t outer,
-               uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer) {
-    const uint64_t dims[2] = {inner, outer};
-    const uint64_t strides[1] = {row_bytes};
-    const uint32_t box[2] = {box_inner, box_outer};
-    return encode(map, dt, base, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
-}
-
-// LHS scales, MN-major: 2-D {rows, kb} with row pitch ld (dense, contiguous) or
-// 3-D {M_cap, kb, G} (masked); each load brings the 128 scales of one K block.
-bool encode_scales_a(CUtensorMap *map, const float *sA, int ld, int rows, int kb, int groups, bool masked) {
-    const uint64_t dims[3] = {(uint64_t)rows, (uint64_t)kb, (uint64_t)groups};
-    const uint64_t strides[2] = {(uint64_t)ld * 4, (uint64_t)ld * 4 * (uint64_t)kb};
-    const uint32_t box[3] = {(uint32_t)fg::BLOCK_M, 1, 1};
-    return encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, sA, masked ? 3 : 2, dims, strides, box,
-                  CU_TENSOR_MAP_SWIZZLE_NONE);
-}
-
-bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
-int cdiv(int a, int b) { return (a + b - 1) / b; }
-
-std::atomic<int> g_force_bn{0};
-std::atomic<int> g_pdl{1};  // programmatic dependent launch of the GEMM kernels
-std::atomic<int> g_force_split{0};
-std::atomic<int> g_pair_mode{-1};  // CTA-pair tiles: -1 where they apply, 0 never, 1 whenever allowed
-
-// Launch helper of one kernel instantiation F with BYTES of dynamic shared
-// memory; CLUSTERED kernels always carry a cluster dimension.
-template <auto F, int BYTES, bool CLUSTERED>
-struct Launcher {
-    // launch configuration: a cluster dimension and/or programmatic dependent
-    // launch (`at` holds room for two attributes)
-    static cudaLaunchConfig_t config(int grid, int cluster, cudaStream_t stream, cudaLaunchAttribute *at,
-                                     bool pdl = false) {
-        cudaLaunchConfig_t cfg{};
-        cfg.gridDim = dim3(grid, 1, 1);
-        cfg.blockDim = dim3(fg::NUM_THREADS, 1, 1);
-        cfg.dynamicSmemBytes = BYTES;
-        cfg.stream = stream;
-        unsigned n = 0;
-        if (cluster > 1 || CLUSTERED) {
-            at[n].id = cudaLaunchAttributeClusterDimension;
-            at[n].val.clusterDim.x = cluster;
-            at[n].val.clusterDim.y = 1;
-            at[n].val.clusterDim.z = 1;
-            ++n;
-        }
-        if (pdl) {
-            at[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-            at[n].val.programmaticStreamSerializationAllowed = 1;
-            ++n;
-        }
-        cfg.attrs = at;
-        cfg.numAttrs = n;
-        return cfg;
-    }
-
-    // dynamic shared memory attribute, once per device
-    static bool configure() {
-        static std::atomic<uint64_t> configured{0};
-        int dev = 0;
-        if (cudaGetDevice(&dev) != cudaSuccess) return false;
-        const uint64_t bit = 1ull << (dev & 63);
-        if (configured.load(std::memory_order_acquire) & bit) return true;
-        if (cudaFuncSetAttribute(F, cudaFuncAttributeMaxDynamicSharedMemorySize, BYTES) != cudaSuccess)
-            return false;
-        configured.fetch_or(bit, std::memory_order_acq_rel);
-        return true;
-    }
-
-    // clusters of `cluster` CTAs that can be resident at once (one wave)
-    static int max_active_clusters(int cluster) {
-        static std::atomic<int> cache[kMaxDevices][9];
-        int dev = 0;
-        if (cluster < 1 || cluster > 8 || cudaGetDevice(&dev) != cudaSuccess || dev >= kMaxDevices) return 0;
-        const int v = cache[dev][cluster].load();
-        if (v > 0) return v;
-        if (!configure()) return 0;
-        cudaLaunchAttribute at[2];
-        cudaLaunchConfig_t cfg = config(cluster, cluster, nullptr, at);
-        int n = 0;
-        if (cudaOccupancyMaxActiveClusters(&n, F, &cfg) != cudaSuccess) {
-            cudaGetLastError();
-            return 0;
-        }
-        cache[dev][cluster].store(n);
-        return n;
-    }
-
-    static fg_status launch(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &td,
-                            const CUtensorMap &tsa, const GemmParams &p, int grid, int cluster,
-                            cudaStream_t stream) {
-        if (!configure()) return cuda_fail();
-        cudaLaunchAttribute at[2];
-        cudaLaunchConfig_t cfg = config(grid, cluster, stream, at, g_pdl.load() != 0);
-        if (cudaLaunchKernelEx(&cfg, F, ta, tb, td, tsa, p) != cudaSuccess) return cuda_fail();
-        return cudaPeekAtLastError() == cudaSuccess ? FG_OK : cuda_fail();
-    }
-};
+using namespace fgh;
 
 template <int BN, int STAGES, int KIND, bool SPLITK, bool F32OUT = false>
 using Kernel =
@@ -344,6 +212,13 @@ fg_status run(const void *A, int a_fmt, const float *sA, int ld_sA, const void *
     int sms = dev->num_sms;
     const int ovr = g_num_sms_override.load();
     if (ovr > 0 && ovr < sms) sms = ovr;
+    if constexpr (KIND != fg::KIND_CONTIGUOUS) {
+        // few rows per group: the weights in the MMA's 128-row role (swap.cu)
+        SwapPlan sp;
+        if (swap_applies(KIND, rows, G, n, k, sms, &sp))
+            return launch_swap(KIND, F32OUT, sp, A, a_fmt, sA, ld_sA, B, b_fmt, sB, D, masked_m, rows, G, n, k, sms,
+                               dev, stream);
+    }
     const int num_kb = cdiv(k, fg::BLOCK_K);
     const long long m_blocks_total = (long long)cdiv(rows, fg::BLOCK_M) * (KIND == fg::KIND_MASKED ? G : 1);
     const Plan plan = choose_plan(m_blocks_total, KIND == fg::KIND_DENSE ? rows : INT32_MAX, n, k, sms);
@@ -685,9 +560,41 @@ fg_status fg_query_dense_plan_ex(int m, int n, int k, int *block_n, int *split_k
     return FG_OK;
 }
 
+fg_status fg_query_plan(int kind, int rows, int G, int n, int k, int *plan) {
+    if (!plan || rows < 1 || G < 1 || n < 1 || k < 1 || kind < fg::KIND_DENSE || kind > fg::KIND_MASKED)
+        return FG_ERR_INVALID_ARG;
+    if (kind == fg::KIND_DENSE && G != 1) return FG_ERR_INVALID_ARG;
+    DeviceInfo *dev = nullptr;
+    if (fg_status st = device_info(&dev); st != FG_OK) return st;
+    int sms = dev->num_sms;
+    const int ovr = g_num_sms_override.load();
+    if (ovr > 0 && ovr < sms) sms = ovr;
+    SwapPlan sp;
+    if (kind != fg::KIND_CONTIGUOUS && swap_applies(kind, rows, G, n, k, sms, &sp)) {
+        plan[0] = sp.bt;
+        plan[1] = sp.split;
+        plan[2] = 0;
+        plan[3] = 1;
+        return FG_OK;
+    }
+    const long long m_blocks = (long long)cdiv(rows, fg::BLOCK_M) * (kind == fg::KIND_MASKED ? G : 1);
+    const Plan p = choose_plan(m_blocks, kind == fg::KIND_DENSE ? rows : INT32_MAX, n, k, sms);
+    plan[0] = p.bn;
+    plan[1] = p.split;
+    plan[2] = use_pair(kind, p, rows) && sms >= 2 ? 1 : 0;
+    plan[3] = 0;
+    return FG_OK;
+}
+
 fg_status fg_set_pair_mode(int mode) {
     if (mode < -1 || mode > 1) return FG_ERR_INVALID_ARG;
     g_pair_mode.store(mode);
+    return FG_OK;
+}
+
+fg_status fg_set_swap_mode(int mode) {
+    if (mode < -1 || mode > 1) return FG_ERR_INVALID_ARG;
+    g_swap_mode.store(mode);
     return FG_OK;
 }
 

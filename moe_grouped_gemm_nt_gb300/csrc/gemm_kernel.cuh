@@ -228,8 +228,8 @@ __device__ __forceinline__ Tile get_tile(const GemmParams &p, int t, int mblocks
     return ti;
 }
 
-__device__ __noinline__ bool wait_phase_slow(uint32_t bar, uint32_t parity, volatile uint32_t *abort_flag,
-                                             const GemmParams &p, uint32_t role);
+static __device__ __noinline__ bool wait_phase_slow(uint32_t bar, uint32_t parity, volatile uint32_t *abort_flag,
+                                                    const GemmParams &p, uint32_t role);
 
 // Bounded wait on an mbarrier phase.  Returns false on watchdog expiry (after
 // recording it and raising the CTA abort flag) or when another role aborted.
@@ -242,8 +242,8 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volati
     return wait_phase_slow(bar, parity, abort_flag, p, role);
 }
 
-__device__ __noinline__ bool wait_phase_slow(uint32_t bar, uint32_t parity, volatile uint32_t *abort_flag,
-                                             const GemmParams &p, uint32_t role) {
+static __device__ __noinline__ bool wait_phase_slow(uint32_t bar, uint32_t parity, volatile uint32_t *abort_flag,
+                                                    const GemmParams &p, uint32_t role) {
     const uint64_t t0 = global_timer_ns();
     uint32_t spins = 0;
     while (!mbar_try_wait(bar, parity)) {
@@ -799,17 +799,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         tc_fence_after();
         tmem_dealloc(tmem_base, L::TMEM_COLS);
     }
-}
-
-// Row-major [batches][rows][kb] -> MN-major [batches][kb][ld] (zero padding).
-__global__ void scales_to_mn_major_kernel(const float *__restrict__ src, float *__restrict__ dst, int rows,
-                                          int kb, int ld) {
-    const int r = blockIdx.x * blockDim.x + threadIdx.x;
-    const int j = blockIdx.y;
-    const size_t b = blockIdx.z;
-    if (r >= ld) return;
-    const float v = r < rows ? src[(b * rows + r) * kb + j] : 0.f;
-    dst[(b * kb + j) * ld + r] = v;
 }
 
 }  // namespace fg
