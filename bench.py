@@ -66,11 +66,20 @@ def sweep_problems():
     return probs, shapes
 
 
-def kernel_name(block_n, split, pair=0):
+def kernel_name(block_n, split, pair=0, swap=0, defer=0):
     if pair:
+        if defer:
+            return "fg::fp8_gemm_pair_kernel<dense,4,8,deferred stores> (256x256 tiles on CTA pairs)"
         return "fg::fp8_gemm_pair_kernel<dense,5,8> (256x256 tiles on CTA pairs)"
+    if swap:
+        return f"fg::fp8_gemm_swap_kernel<{block_n},dense,{'splitk' if split > 1 else 'persistent'}>"
     stages = 4 if block_n == 256 else 6
     return f"fg::fp8_gemm_kernel<{block_n},{stages},dense,{'splitk' if split > 1 else 'persistent'}>"
+
+
+def plan_of(fg, m, n, k):
+    """(block_n, split_k, cta_pair, swap_ab, deferred_stores) of a dense call."""
+    return tuple(fg.fg_query_plan(0, m, 1, n, k))
 
 
 def kernel_sources_digest():
@@ -493,8 +502,7 @@ def run_ours(args, ws, rank, local):
     # group boundary gives every kernel's device time inside the timed region.
     groups = {}
     for i, (m, n, k, _) in enumerate(items):
-        bn, split, pair = fg.fg_query_dense_plan_ex(m, n, k)
-        groups.setdefault(kernel_name(bn, split, pair), []).append(i)
+        groups.setdefault(kernel_name(*plan_of(fg, m, n, k)), []).append(i)
     group_names = list(groups)
     group_items = [groups[g] for g in group_names]
 
@@ -588,10 +596,9 @@ def run_ours(args, ws, rank, local):
                            "frac_hbm_peak": round(b / t / 1e9 / hbm_peak, 3),
                            "roofline_over_time": round(t_roof / t, 3)})
     for r in shape_rows:
-        bn, split, pair = fg.fg_query_dense_plan_ex(r["m"], r["n"], r["k"])
-        r["plan"] = {"block_n": bn, "split_k": split}
-        r["plan"]["cta_pair"] = pair
-        r["kernel"] = kernel_name(bn, split, pair)
+        pl = plan_of(fg, r["m"], r["n"], r["k"])
+        r["plan"] = {"block_n": pl[0], "split_k": pl[1], "cta_pair": pl[2], "swap_ab": pl[3], "deferred_stores": pl[4]}
+        r["kernel"] = kernel_name(*pl)
     traffic_tab = load_traffic()
     ridge = fp8_peak * 1e12 / (hbm_peak * 1e9)
 

@@ -257,10 +257,13 @@ fg_status fg_set_swap_mode(int mode);
 
 /* The tile plan a call of this layout and shape would use on the current
  * device.  kind: 0 dense (rows = m, G = 1), 1 contiguous (rows = M), 2 masked
- * (rows = M_cap).  plan[4] receives: [0] the tile width (output columns per
+ * (rows = M_cap).  plan[5] receives: [0] the tile width (output columns per
  * tile; with swapped roles, rows of A per tile), [1] the split-K cluster size
- * (1 = none), [2] 1 for CTA-pair tiles, [3] 1 for swapped operand roles.
- * Host-only (reads device attributes, launches nothing). */
+ * (1 = none), [2] 1 for CTA-pair tiles, [3] 1 for swapped operand roles,
+ * [4] 1 when the CTA-pair tiles of a BF16 call stage a whole tile and an
+ * eleventh warp issues its stores (tiles of at most 16 K blocks; the FP32
+ * output forms never do).  Host-only (reads device attributes, launches
+ * nothing). */
 fg_status fg_query_plan(int kind, int rows, int G, int n, int k, int *plan);
 
 /* Programmatic dependent launch of the GEMM kernels (default on): a call's

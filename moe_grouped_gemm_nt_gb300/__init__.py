@@ -61,6 +61,7 @@ SIGNATURES = {
     "fg_status_string": (ctypes.c_char_p, [_I]),
     "fg_version": (_I, []),
     "fg_debug_skip_producer_iteration": (_I, [_I]),
+    "fg_debug_set_pair_defer": (_I, [_I]),
 }
 
 
@@ -390,8 +391,9 @@ def fg_set_swap_mode(mode: int) -> None:
 
 
 def fg_query_plan(kind: int, rows: int, G: int, n: int, k: int):
-    """(tile width, split_k, cta_pair, swap_ab) of a call: kind 0 dense, 1 contiguous, 2 masked."""
-    pl = (ctypes.c_int * 4)()
+    """(tile width, split_k, cta_pair, swap_ab, deferred_stores) of a call: kind 0 dense, 1 contiguous,
+    2 masked."""
+    pl = (ctypes.c_int * 5)()
     _check("fg_query_plan", lib().fg_query_plan(int(kind), int(rows), int(G), int(n), int(k), pl))
     return tuple(pl)
 

@@ -75,6 +75,19 @@ constexpr int kPairScaleStages = 8;
 template <int KIND, bool F32OUT = false>
 using PairKernel = Launcher<fg::fp8_gemm_pair_kernel<KIND, kPairStages, kPairScaleStages, F32OUT>,
                             fg::PairSmemLayout<kPairStages, kPairScaleStages>::BYTES, true>;
+// deferred stores (BF16 output): the staging holds a whole tile, bought with
+// one operand stage less
+constexpr int kPairDeferStages = 4;
+template <int KIND>
+using PairDeferKernel = Launcher<fg::fp8_gemm_pair_kernel<KIND, kPairDeferStages, kPairScaleStages, false, true>,
+                                 fg::PairSmemLayout<kPairDeferStages, kPairScaleStages, true>::BYTES, true,
+                                 fg::PAIR_DEFER_THREADS>;
+// -1: deferred stores for tiles of at most kPairDeferMaxKb K blocks (measured:
+// 4096 x 24576 x 1536 137.8 -> 128.9 us, 4096 x 7168 x 2048 56.0 -> 54.1 us;
+// with 56 or more K blocks the fifth operand stage is worth more: 4096 x 7168
+// x 16384 333.8 -> 340.5 us); 0 never; 1 always
+std::atomic<int> g_pair_defer{-1};
+constexpr int kPairDeferMaxKb = 16;
 
 // Tile plan of one call: output tile width and split-K factor.
 struct Plan {
@@ -265,10 +278,16 @@ fg_status run(const void *A, int a_fmt, const float *sA, int ld_sA, const void *
             p.group_m = raster_group_m(KIND, (int)pblocks, 2 * k);
             p.idesc = fg::make_idesc_f8f6f4(fg::PAIR_ROWS, fg::PAIR_BN, (uint32_t)a_fmt, (uint32_t)b_fmt);
             const long long tiles = pblocks * p.num_n_blocks;
-            long long clusters = PairKernel<KIND, F32OUT>::max_active_clusters(2);
+            const int dmode = g_pair_defer.load();
+            const bool defer = !F32OUT && (dmode == 1 || (dmode < 0 && num_kb <= kPairDeferMaxKb));
+            long long clusters = defer ? PairDeferKernel<KIND>::max_active_clusters(2)
+                                       : PairKernel<KIND, F32OUT>::max_active_clusters(2);
             if (clusters < 1) return cuda_fail();
             if (clusters > sms / 2) clusters = sms / 2;  // the SM limit (fg_set_num_sms); sms >= 2 here
             if (clusters > tiles) clusters = tiles;
+            if constexpr (!F32OUT) {
+                if (defer) return PairDeferKernel<KIND>::launch(ta, tb, td, tsa, p, (int)(2 * clusters), 2, stream);
+            }
             return PairKernel<KIND, F32OUT>::launch(ta, tb, td, tsa, p, (int)(2 * clusters), 2, stream);
         }
     }
@@ -570,6 +589,7 @@ fg_status fg_query_plan(int kind, int rows, int G, int n, int k, int *plan) {
     const int ovr = g_num_sms_override.load();
     if (ovr > 0 && ovr < sms) sms = ovr;
     SwapPlan sp;
+    plan[4] = 0;
     if (kind != fg::KIND_CONTIGUOUS && swap_applies(kind, rows, G, n, k, sms, &sp)) {
         plan[0] = sp.bt;
         plan[1] = sp.split;
@@ -583,6 +603,8 @@ fg_status fg_query_plan(int kind, int rows, int G, int n, int k, int *plan) {
     plan[1] = p.split;
     plan[2] = use_pair(kind, p, rows) && sms >= 2 ? 1 : 0;
     plan[3] = 0;
+    const int dmode = g_pair_defer.load();
+    plan[4] = plan[2] && (dmode == 1 || (dmode < 0 && cdiv(k, fg::BLOCK_K) <= kPairDeferMaxKb)) ? 1 : 0;
     return FG_OK;
 }
 
@@ -621,6 +643,16 @@ fg_status fg_set_watchdog_ms(uint32_t ms) {
 // warp's bounded wait expires and the call reports FG_ERR_TIMEOUT; in the next
 // quantization call, every CTA's producer leaves its unit number `iter`
 // unfilled, with the same outcome for the consumer warps.
+// Test and measurement hook (not part of the public header): CTA-pair tiles
+// with BF16 output stage a whole tile and let an eleventh warp issue its
+// stores (1), stage box by box and store from the promotion warps (0), or
+// choose by the number of K blocks (-1, the default).
+fg_status fg_debug_set_pair_defer(int mode) {
+    if (mode < -1 || mode > 1) return FG_ERR_INVALID_ARG;
+    g_pair_defer.store(mode);
+    return FG_OK;
+}
+
 fg_status fg_debug_skip_producer_iteration(int iter) {
     g_debug_skip_iter.store(iter);
     return FG_OK;

@@ -33,18 +33,26 @@ namespace fg {
 constexpr int PAIR_BN = 256;         // N of the pair tile = columns of each CTA's accumulator
 constexpr int PAIR_ROWS = 2 * BLOCK_M;  // M of the pair tile
 
-template <int STAGES, int SS>
+// Deferred stores (DEFER): an eleventh warp issues the epilogue's TMA stores, so
+// the promotion warps stage a whole tile (both 64-column boxes of each warp)
+// and go straight on to the next tile.
+constexpr int STORE_WARP = 10;
+constexpr int PAIR_DEFER_THREADS = 352;
+
+template <int STAGES, int SS, bool DEFER = false>
 struct PairSmemLayout {
     static constexpr int HB_STAGE_BYTES = (PAIR_BN / 2) * BLOCK_K;  // this CTA's half of B
+    static constexpr int STG_PER_WARP = DEFER ? 2 * STAGING_BYTES_PER_WARP : STAGING_BYTES_PER_WARP;
     static constexpr int A_OFF = 0;
     static constexpr int B_OFF = A_OFF + STAGES * A_STAGE_BYTES;
     static constexpr int STG_OFF = B_OFF + STAGES * HB_STAGE_BYTES;
-    static constexpr int SA_OFF = STG_OFF + NUM_EPI_WARPS * STAGING_BYTES_PER_WARP;
+    static constexpr int SA_OFF = STG_OFF + NUM_EPI_WARPS * STG_PER_WARP;
     static constexpr int SB_OFF = SA_OFF + SS * SA_STAGE_BYTES;
     static constexpr int BAR_OFF = SB_OFF + SS * SB_STAGE_BYTES;
     static constexpr int NUM_TBUF = 2;
     // full, empty, scale_full, scale_empty, tmem_full, tmem_empty, drain
-    static constexpr int NUM_BARS = 2 * STAGES + 2 * SS + 2 * NUM_TBUF + 1;
+    // (DEFER: + staging_full, staging_empty)
+    static constexpr int NUM_BARS = 2 * STAGES + 2 * SS + 2 * NUM_TBUF + 1 + (DEFER ? 2 : 0);
     static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
     static constexpr int BYTES = MISC_OFF + 16;
     static constexpr int TMEM_COLS = 512;
@@ -115,15 +123,17 @@ __device__ __forceinline__ PairTile get_pair_tile(const GemmParams &p, int t, in
 
 // Tensor maps: A [rows][k] u8 (box 128 rows), B [G*n][k] u8 (box 128 rows: one
 // CTA's half of the pair tile's 256), D [rows][n] bf16 or (F32OUT) fp32, SA as
-// for the one-CTA kernel.  Launched with clusters of 2 CTAs.
-template <int KIND, int STAGES, int SS, bool F32OUT>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+// for the one-CTA kernel.  Launched with clusters of 2 CTAs (DEFER: 352
+// threads per CTA, the eleventh warp issuing the epilogue's stores).
+template <int KIND, int STAGES, int SS, bool F32OUT, bool DEFER = false>
+__global__ void __launch_bounds__(DEFER ? PAIR_DEFER_THREADS : NUM_THREADS, 1)
     fp8_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                          const __grid_constant__ CUtensorMap tmap_d, const __grid_constant__ CUtensorMap tmap_sa,
                          const GemmParams p) {
     static_assert(KIND == KIND_DENSE || KIND == KIND_MASKED, "pair tiles: dense and masked layouts");
     static_assert((SS & (SS - 1)) == 0, "scale ring size");
-    using L = PairSmemLayout<STAGES, SS>;
+    static_assert(!(DEFER && F32OUT), "deferred stores: BF16 output");
+    using L = PairSmemLayout<STAGES, SS, DEFER>;
     constexpr int BN = PAIR_BN;
     constexpr int COLS = BN / 2;  // columns per promotion warp
     constexpr uint32_t NTB = L::NUM_TBUF;
@@ -142,6 +152,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     auto tfull_bar = [&](uint32_t b) { return bar0 + 8u * (2 * STAGES + 2 * SS + b); };
     auto tempty_bar = [&](uint32_t b) { return bar0 + 8u * (2 * STAGES + 2 * SS + NTB + b); };
     const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 2 * SS + 2 * NTB);
+    const uint32_t stg_full_bar = drain_bar + 8u;    // DEFER: the tile's boxes are staged
+    const uint32_t stg_empty_bar = drain_bar + 16u;  // DEFER: their stores have read the staging
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::MISC_OFF);
     volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(smem + L::MISC_OFF + 4);
 
@@ -177,6 +189,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 mbar_init(tempty_bar(b), 2 * NUM_EPI_WARPS);  // both CTAs' promotion warps
             }
             mbar_init(drain_bar, 1);
+            if constexpr (DEFER) {
+                mbar_init(stg_full_bar, NUM_EPI_WARPS);
+                mbar_init(stg_empty_bar, 1);
+            }
             *abort_flag = 0u;
             fence_mbarrier_init();
         }
@@ -304,12 +320,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int sub = warp & 3;
         const int half = warp >> 2;
         const int r = sub * 32 + lane;
-        const uint32_t stg = sbase + L::STG_OFF + warp * STAGING_BYTES_PER_WARP;
+        const uint32_t stg = sbase + L::STG_OFF + warp * L::STG_PER_WARP;
         const uint32_t t_lane = (uint32_t)(sub * 32) << 16;
         const uint32_t sa_addr = sbase + L::SA_OFF + r * 4;
         const uint32_t sb_addr = sbase + L::SB_OFF + half * 4;
         const uint32_t t_base = tmem_base + t_lane + half * COLS;
         uint32_t b = 0, bph = 0, q = 0, qph = 0;
+        uint32_t ep = 0;  // DEFER: tiles staged so far (parity of the staging barriers)
         bool ok = true;
         for (int t = t_begin; t < num_tiles && ok; t += t_step) {
             const PairTile ti = get_pair_tile<KIND>(p, t, pblocks, rank);
@@ -373,7 +390,28 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 use_tma = true;  // rows past m are clipped by the tensor map bounds
             else
                 use_tma = __all_sync(0xffffffffu, row_ok);
-            if (use_tma) {
+            if constexpr (DEFER) {
+                // the store warp has finished reading the previous tile's staging
+                // (every warp waits, so none can be a tile ahead of the others)
+                if (!__all_sync(0xffffffffu,
+                                wait_phase(stg_empty_bar, (ep & 1u) ^ 1u, abort_flag, p, ROLE_EPILOGUE)))
+                    break;
+                ++ep;
+            }
+            if (DEFER && use_tma) {
+                // stage both 64-column boxes; the store warp issues their stores
+#pragma unroll
+                for (int bx = 0; bx < COLS / 64; ++bx) {
+#pragma unroll
+                    for (int ch = 0; ch < 8; ++ch) {
+                        const float *f = acc + bx * 64 + ch * 8;
+                        const uint32_t off = (uint32_t)lane * 128u + ((uint32_t)(ch ^ (lane & 7)) << 4);
+                        st_shared_v4(stg + bx * STAGING_BYTES_PER_WARP + off, pack_bf16x2(f[0], f[1]),
+                                     pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]), pack_bf16x2(f[6], f[7]));
+                    }
+                }
+                fence_proxy_async_smem();
+            } else if (use_tma) {
                 if constexpr (F32OUT) {
                     // FP32 boxes: 32 rows x 32 columns (128 bytes per row, same swizzle)
 #pragma unroll
@@ -445,8 +483,45 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     }
                 }
             }
+            if constexpr (DEFER) {
+                __syncwarp();
+                if (lane == 0) mbar_arrive(stg_full_bar);  // this warp's part of the tile is staged (or stored)
+            }
         }
         if (lane == 0) bulk_wait_group<0>();
+        __syncwarp();
+    } else if (DEFER && warp == STORE_WARP) {
+        // ------------------------------------------------ store warp (DEFER)
+        // Walks the same tiles; once all promotion warps have staged a tile it
+        // issues the TMA stores of the boxes they would have stored (same
+        // predicates), waits until the stores have read the staging and hands
+        // it back.
+        if (lane == 0) {
+            uint32_t ep = 0;
+            for (int t = t_begin; t < num_tiles; t += t_step) {
+                const PairTile ti = get_pair_tile<KIND>(p, t, pblocks, rank);
+                if (!ti.valid) continue;
+                if (!wait_phase(stg_full_bar, ep & 1u, abort_flag, p, ROLE_EPILOGUE)) break;
+                ++ep;
+                for (int w = 0; w < NUM_EPI_WARPS; ++w) {
+                    const int wsub = w & 3, whalf = w >> 2;
+                    const bool rows_in = wsub * 32 < ti.row_limit;
+                    const bool all_rows = KIND == KIND_DENSE || wsub * 32 + 32 <= ti.row_limit;
+                    if (!rows_in || !all_rows) continue;  // nothing staged, or stored row by row
+                    const int d_row = ti.a_row + wsub * 32;
+                    for (int bx = 0; bx < COLS / 64; ++bx) {
+                        const int x = ti.n_blk * BN + whalf * COLS + bx * 64;
+                        if (x >= p.n) continue;
+                        tma_store_2d(&tmap_d, sbase + L::STG_OFF + w * L::STG_PER_WARP + bx * STAGING_BYTES_PER_WARP,
+                                     x, d_row);
+                    }
+                }
+                bulk_commit_group();
+                bulk_wait_group_read<0>();
+                mbar_arrive(stg_empty_bar);
+            }
+            bulk_wait_group<0>();
+        }
         __syncwarp();
     }
 

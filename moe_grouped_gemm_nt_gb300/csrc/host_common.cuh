@@ -157,7 +157,7 @@ inline int cdiv(int a, int b) { return (a + b - 1) / b; }
 
 // Launch helper of one kernel instantiation F with BYTES of dynamic shared
 // memory; CLUSTERED kernels always carry a cluster dimension.
-template <auto F, int BYTES, bool CLUSTERED>
+template <auto F, int BYTES, bool CLUSTERED, int THREADS = fg::NUM_THREADS>
 struct Launcher {
     // launch configuration: a cluster dimension and/or programmatic dependent
     // launch (`at` holds room for two attributes)
@@ -165,7 +165,7 @@ struct Launcher {
                                      bool pdl = false) {
         cudaLaunchConfig_t cfg{};
         cfg.gridDim = dim3(grid, 1, 1);
-        cfg.blockDim = dim3(fg::NUM_THREADS, 1, 1);
+        cfg.blockDim = dim3(THREADS, 1, 1);
         cfg.dynamicSmemBytes = BYTES;
         cfg.stream = stream;
         unsigned n = 0;

@@ -249,6 +249,32 @@ def test_pair_plan_query():
 
     assert fg.fg_query_dense_plan_ex(4096, 7168, 2048)[2] == 1
     assert fg.fg_query_dense_plan_ex(128, 7168, 2048)[2] == 0
+    # BF16 pair tiles of at most 16 K blocks store through the eleventh warp
+    assert fg.fg_query_plan(0, 4096, 1, 7168, 2048)[2:] == (1, 0, 1)
+    assert fg.fg_query_plan(0, 4096, 1, 7168, 16384)[2:] == (1, 0, 0)
+
+
+@pytest.mark.parametrize("m,n,k", [(640, 2112, 1536), (300, 520, 2048), (1030, 1800, 640), (512, 768, 4096)])
+def test_pair_deferred_stores_are_bitwise_the_same(pair_mode, m, n, k):
+    """Staging a whole tile and storing it from the eleventh warp changes only
+    who issues the TMA stores: the bits equal those of the promotion warps'
+    own stores, dense and masked, short and long K."""
+    import moe_grouped_gemm_nt_gb300 as fg
+    from gpu_common import run_masked
+
+    pair_mode(1)
+    p = wl.dense(m, n, k, seed=9150 + m + k)
+    q = wl.masked(3, 512, n=n, k=k, seed=9160 + k, masked_m=[0, 300, 512])
+    outs = []
+    try:
+        for mode in (0, 1):
+            assert fg.lib().fg_debug_set_pair_defer(mode) == 0
+            outs.append((d_to_bits(run_dense(p)), d_to_bits(run_masked(q))))
+    finally:
+        fg.lib().fg_debug_set_pair_defer(-1)
+    assert np.array_equal(outs[0][0], outs[1][0]) and np.array_equal(outs[0][1], outs[1][1])
+    ref16, _ = oracle.gemm_fp8_nt(p.A, 0, p.sA, p.B, 0, p.sB, want_f64=False)
+    compare(outs[1][0], ref16, what=f"deferred stores {m}x{n}x{k}")
 
 
 @pytest.mark.parametrize("mode,bn,split", [("pair", 0, 0), ("one_cta", 256, 1), ("split", 128, 4)])

@@ -19,16 +19,19 @@ if not torch.cuda.is_available():
 from gpu_common import compare, d_to_bits, dev, fp8_dtype, run_dense  # noqa: E402
 
 
-@pytest.fixture(params=[0, 1], ids=["one_cta", "cta_pair"])
+@pytest.fixture(params=[0, 1, 2], ids=["one_cta", "cta_pair_deferred_stores", "cta_pair"])
 def short_watchdog(request):
-    """Persistent 128x256 tiles on one CTA, or 256x256 tiles on CTA pairs."""
+    """Persistent 128x256 tiles on one CTA, or 256x256 tiles on CTA pairs
+    (with the store warp, or with the promotion warps storing)."""
     fg.fg_set_watchdog_ms(200)
     fg.fg_set_config_override(256, 1)
-    fg.fg_set_pair_mode(request.param)
+    fg.fg_set_pair_mode(1 if request.param else 0)
+    fg.lib().fg_debug_set_pair_defer(1 if request.param == 1 else 0)
     yield
     fg.fg_set_watchdog_ms(0)
     fg.fg_set_config_override(0, 0)
     fg.fg_set_pair_mode(-1)
+    fg.lib().fg_debug_set_pair_defer(-1)
     fg.lib().fg_debug_skip_producer_iteration(-1)
 
 
