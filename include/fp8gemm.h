@@ -143,7 +143,12 @@ fg_status fg_grouped_gemm_fp8_masked_f32out(const void *A, int a_fmt, const floa
  *       walk rounds it down / clips it to K.
  *   D   [G][M][N] bfloat16 (the _f32out form: float), 16-byte aligned; every
  *       element is written (an empty segment gives zeros).
- * K % 16 == 0, N % 8 == 0; M == 0 is a no-op. */
+ * K % 16 == 0, N % 8 == 0; M == 0 is a no-op.  Tiles: for the BF16 form
+ * with M >= 256 and segments of at most 16 K blocks on average, 256 x 256 on
+ * CTA pairs (with the store warp from 4 K blocks on average; measured faster
+ * there, while one-CTA tiles are faster on longer segments), else 128 x 256
+ * or, when those would leave SMs idle, 128 x 128 on one CTA; fg_query_plan
+ * with kind 3 reports the choice. */
 fg_status fg_k_grouped_gemm_fp8_nt(const void *A, int a_fmt, const float *sA, int ld_sA,
                                    const void *B, int b_fmt, const float *sB, void *D,
                                    const int32_t *k_sizes, int G, int M, int N, int K, void *stream);
@@ -229,8 +234,9 @@ fg_status fg_query_dense_plan(int m, int n, int k, int *block_n, int *split_k);
 fg_status fg_query_dense_plan_ex(int m, int n, int k, int *block_n, int *split_k, int *cta_pair);
 
 /* CTA-pair tiles for later calls: -1 (default) where they apply (persistent
- * 256-wide dense plans with at least 256 rows, no forced plan), 0 never, 1 for
- * every persistent 256-wide dense or masked plan.  The contiguous layout
+ * 256-wide dense plans with at least 256 rows, K-grouped BF16 calls with short
+ * segments as described there; no forced plan), 0 never, 1 for every
+ * persistent 256-wide dense, masked or K-grouped plan.  The contiguous layout
  * always uses 128-row tiles (two adjacent 128-row blocks may belong to two
  * groups; measured, pairing them with a second pass for such blocks was
  * slower than 128-row tiles).  The masked layout uses 128-row tiles unless
@@ -257,13 +263,13 @@ fg_status fg_set_swap_mode(int mode);
 
 /* The tile plan a call of this layout and shape would use on the current
  * device.  kind: 0 dense (rows = m, G = 1), 1 contiguous (rows = M), 2 masked
- * (rows = M_cap).  plan[5] receives: [0] the tile width (output columns per
- * tile; with swapped roles, rows of A per tile), [1] the split-K cluster size
- * (1 = none), [2] 1 for CTA-pair tiles, [3] 1 for swapped operand roles,
- * [4] 1 when the CTA-pair tiles of a BF16 call stage a whole tile and an
- * eleventh warp issues its stores (tiles of at most 16 K blocks; the FP32
- * output forms never do).  Host-only (reads device attributes, launches
- * nothing). */
+ * (rows = M_cap), 3 K-grouped (rows = M, n = N, k = K).  plan[5] receives:
+ * [0] the tile width (output columns per tile; with swapped roles, rows of A
+ * per tile), [1] the split-K cluster size (1 = none), [2] 1 for CTA-pair
+ * tiles, [3] 1 for swapped operand roles, [4] 1 when the CTA-pair tiles of a
+ * BF16 call stage a whole tile and a store warp issues its stores (tiles of
+ * at most 16 K blocks, K-grouped: 4 to 16 on average; the FP32 output forms
+ * never do).  Host-only (reads device attributes, launches nothing). */
 fg_status fg_query_plan(int kind, int rows, int G, int n, int k, int *plan);
 
 /* Programmatic dependent launch of the GEMM kernels (default on): a call's

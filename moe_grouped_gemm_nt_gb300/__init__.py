@@ -392,7 +392,7 @@ def fg_set_swap_mode(mode: int) -> None:
 
 def fg_query_plan(kind: int, rows: int, G: int, n: int, k: int):
     """(tile width, split_k, cta_pair, swap_ab, deferred_stores) of a call: kind 0 dense, 1 contiguous,
-    2 masked."""
+    2 masked, 3 K-grouped (rows = M, n = N, k = K)."""
     pl = (ctypes.c_int * 5)()
     _check("fg_query_plan", lib().fg_query_plan(int(kind), int(rows), int(G), int(n), int(k), pl))
     return tuple(pl)

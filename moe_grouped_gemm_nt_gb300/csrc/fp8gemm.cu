@@ -313,8 +313,40 @@ fg_status run(const void *A, int a_fmt, const float *sA, int ld_sA, const void *
 
 // K-grouped entry points: G groups, each an NT product over its own segment of
 // K (segment lengths on the device), all sharing A [M][K] and B [N][K]; output
-// planes D [G][M][N].  Persistent one-CTA tiles (128 x 256, or 128 x 128 when
-// the 256-wide tiles would leave SMs idle), no split-K.
+// planes D [G][M][N].  Persistent tiles, no split-K: 256 x 256 on CTA pairs
+// with the store warp for short segments (BF16 output, M >= 256, the 256-wide
+// tiles filling the SMs), else one-CTA 128 x 256 (or 128 x 128 when the
+// 256-wide tiles would leave SMs idle).
+struct KgPlan {
+    int bn = 256;
+    bool pair = false;
+    bool defer = false;  // CTA pairs with the store warp (BF16 output only)
+};
+KgPlan kgrouped_plan(int G, int M, int N, int K, int sms, bool f32out) {
+    KgPlan kp;
+    // 256-wide tiles unless they fill less than three quarters of the SMs
+    // four times over and 128-wide ones have more tiles (or the width is forced)
+    const long long tiles256 = (long long)G * cdiv(M, fg::BLOCK_M) * cdiv(N, 256);
+    const int fbn = g_force_bn.load();
+    if (fbn == 128 || (fbn == 0 && tiles256 * 4 < (long long)sms * 3)) kp.bn = 128;
+    // CTA pairs when the segments are short (at most kPairDeferMaxKb K blocks
+    // on average), with the store warp unless they are shorter than 4 K
+    // blocks; one-CTA tiles otherwise.  Measured (BF16 output; one CTA / pairs
+    // / pairs with the store warp): 8 groups of 4096 x 7168 with 1024 tokens
+    // each 253.8 / 264.8 / 238.7 us; 16 of 2048 x 2048 with 512 tokens 52.6 /
+    // 53.9 / 46.8 us; 32 of 4096 x 7168 with 256 tokens 395.8 / 385.6 / 405.2
+    // us; with 8192 tokens per group one-CTA tiles win (8 of 4096 x 7168: 1449
+    // against 1605 / 1633 us).
+    const long long kb_total = cdiv(K, fg::BLOCK_K);
+    const bool short_segments = kb_total <= (long long)kPairDeferMaxKb * G;
+    const int pmode = g_pair_mode.load();
+    kp.pair = sms >= 2 && kp.bn == 256 && pmode != 0 &&
+              (pmode == 1 || (fbn == 0 && M >= fg::PAIR_ROWS && !f32out && short_segments));
+    const int dmode = g_pair_defer.load();
+    kp.defer = kp.pair && !f32out && (dmode == 1 || (dmode < 0 && short_segments && kb_total >= 4ll * G));
+    return kp;
+}
+
 template <bool F32OUT>
 fg_status run_kgrouped(const void *A, int a_fmt, const float *sA, int ld_sA, const void *B, int b_fmt,
                        const float *sB, void *D, const int32_t *k_sizes, int G, int M, int N, int K,
@@ -334,10 +366,9 @@ fg_status run_kgrouped(const void *A, int a_fmt, const float *sA, int ld_sA, con
     int sms = dev->num_sms;
     const int ovr = g_num_sms_override.load();
     if (ovr > 0 && ovr < sms) sms = ovr;
-    // 256-wide tiles unless they fill less than three quarters of the SMs
-    // four times over and 128-wide ones have more tiles (or the width is forced)
-    int BN = 256;
-    if (g_force_bn.load() == 128 || (g_force_bn.load() == 0 && tiles256 * 4 < (long long)sms * 3)) BN = 128;
+    const KgPlan kp = kgrouped_plan(G, M, N, K, sms, F32OUT);
+    const int BN = kp.bn;
+    const bool pair = kp.pair;
 
     const int num_kb = cdiv(K, fg::BLOCK_K);
     CUtensorMap ta, tb, td, tsa;
@@ -348,7 +379,7 @@ fg_status run_kgrouped(const void *A, int a_fmt, const float *sA, int ld_sA, con
         !encode_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, (uint64_t)K, (uint64_t)M, (uint64_t)K, fg::BLOCK_K,
                    fg::BLOCK_M) ||
         !encode_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, (uint64_t)K, (uint64_t)N, (uint64_t)K, fg::BLOCK_K,
-                   (uint32_t)BN) ||
+                   (uint32_t)(pair ? fg::PAIR_BN / 2 : BN)) ||
         !encode(&td, F32OUT ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, D, 3, ddims,
                 dstrides, dbox, CU_TENSOR_MAP_SWIZZLE_128B))
         return cuda_fail();
@@ -362,7 +393,10 @@ fg_status run_kgrouped(const void *A, int a_fmt, const float *sA, int ld_sA, con
     p.num_nb = cdiv(N, 128);
     p.num_n_blocks = cdiv(N, BN);
     p.num_m_blocks = cdiv(M, fg::BLOCK_M);
-    p.group_m = raster_group_m(fg::KIND_KGROUPED, p.num_m_blocks, K);
+    // the raster sizes its L2 working set by the K that one tile reads: the
+    // segments' average length (the lengths stay on the device)
+    const int k_seg = (int)std::max<long long>(fg::BLOCK_K, (long long)cdiv(K, fg::BLOCK_K) * fg::BLOCK_K / G);
+    p.group_m = raster_group_m(fg::KIND_KGROUPED, p.num_m_blocks, k_seg);
     p.idesc = fg::make_idesc_f8f6f4(fg::BLOCK_M, BN, (uint32_t)a_fmt, (uint32_t)b_fmt);
     p.sB = sB;
     p.k_sizes = k_sizes;
@@ -370,6 +404,25 @@ fg_status run_kgrouped(const void *A, int a_fmt, const float *sA, int ld_sA, con
     p.status = dev->status;
     p.timeout_ns = (unsigned long long)g_watchdog_ms.load() * 1000000ull;
     p.debug_skip_iter = g_debug_skip_iter.exchange(-1);
+    if (pair) {
+        // the raster counts 256-row blocks within each group's plane
+        const int pblocks = cdiv(M, fg::PAIR_ROWS);
+        p.num_n_blocks = cdiv(N, fg::PAIR_BN);
+        p.group_m = raster_group_m(fg::KIND_KGROUPED, pblocks, 2 * k_seg);
+        p.idesc = fg::make_idesc_f8f6f4(fg::PAIR_ROWS, fg::PAIR_BN, (uint32_t)a_fmt, (uint32_t)b_fmt);
+        const long long tiles = (long long)G * pblocks * p.num_n_blocks;
+        const bool defer = kp.defer;
+        long long clusters = defer ? PairDeferKernel<fg::KIND_KGROUPED>::max_active_clusters(2)
+                                   : PairKernel<fg::KIND_KGROUPED, F32OUT>::max_active_clusters(2);
+        if (clusters < 1) return cuda_fail();
+        if (clusters > sms / 2) clusters = sms / 2;
+        if (clusters > tiles) clusters = tiles;
+        if constexpr (!F32OUT) {
+            if (defer)
+                return PairDeferKernel<fg::KIND_KGROUPED>::launch(ta, tb, td, tsa, p, (int)(2 * clusters), 2, stream);
+        }
+        return PairKernel<fg::KIND_KGROUPED, F32OUT>::launch(ta, tb, td, tsa, p, (int)(2 * clusters), 2, stream);
+    }
     const long long tiles = (long long)G * p.num_m_blocks * p.num_n_blocks;
     const int grid = (int)(tiles < sms ? tiles : sms);
     if (BN == 128)
@@ -580,7 +633,7 @@ fg_status fg_query_dense_plan_ex(int m, int n, int k, int *block_n, int *split_k
 }
 
 fg_status fg_query_plan(int kind, int rows, int G, int n, int k, int *plan) {
-    if (!plan || rows < 1 || G < 1 || n < 1 || k < 1 || kind < fg::KIND_DENSE || kind > fg::KIND_MASKED)
+    if (!plan || rows < 1 || G < 1 || n < 1 || k < 1 || kind < fg::KIND_DENSE || kind > fg::KIND_KGROUPED)
         return FG_ERR_INVALID_ARG;
     if (kind == fg::KIND_DENSE && G != 1) return FG_ERR_INVALID_ARG;
     DeviceInfo *dev = nullptr;
@@ -588,6 +641,15 @@ fg_status fg_query_plan(int kind, int rows, int G, int n, int k, int *plan) {
     int sms = dev->num_sms;
     const int ovr = g_num_sms_override.load();
     if (ovr > 0 && ovr < sms) sms = ovr;
+    if (kind == fg::KIND_KGROUPED) {
+        const KgPlan kp = kgrouped_plan(G, rows, n, k, sms, false);
+        plan[0] = kp.bn;
+        plan[1] = 1;
+        plan[2] = kp.pair ? 1 : 0;
+        plan[3] = 0;
+        plan[4] = kp.defer ? 1 : 0;
+        return FG_OK;
+    }
     SwapPlan sp;
     plan[4] = 0;
     if (kind != fg::KIND_CONTIGUOUS && swap_applies(kind, rows, G, n, k, sms, &sp)) {

@@ -66,6 +66,7 @@ struct PairTile {
     int sa_row;     // same, as the row coordinate of the scale tensor map
     int b_row;      // first row of this CTA's half of B in the 2-D row space [G*n][k]
     int row_limit;  // rows of this CTA's half below the bound (<= 0: none)
+    int kb_lo, kb_hi;  // K-grouped layout: the tile's K blocks (its group's segment)
 };
 
 // 256-row blocks of the whole walk (masked: of all groups' counts).
@@ -82,10 +83,26 @@ __device__ __forceinline__ int total_pair_blocks(const GemmParams &p) {
 }
 
 // Pair tile t (cluster c takes tiles c, c + clusters, ...), the half of CTA
-// `rank`; the raster is that of get_tile() over 256-row blocks.
+// `rank`; the raster is that of get_tile() over 256-row blocks.  K-grouped
+// layout: the tiles of group g (every 256-row block of its output plane)
+// before those of group g + 1, the K range from the forward scan of get_tile().
 template <int KIND>
-__device__ __forceinline__ PairTile get_pair_tile(const GemmParams &p, int t, int pblocks, uint32_t rank) {
+__device__ __forceinline__ PairTile get_pair_tile(const GemmParams &p, int t, int pblocks, uint32_t rank,
+                                                  KScan &scan) {
     PairTile ti;
+    ti.kb_lo = 0;
+    ti.kb_hi = p.num_kb;
+    ti.group = 0;
+    if constexpr (KIND == KIND_KGROUPED) {
+        const int per_g = pblocks * p.num_n_blocks;
+        const int g = t / per_g;
+        t -= g * per_g;
+        if (g < scan.g) scan = KScan{};
+        while (scan.g < g) scan.kb += k_segment_blocks(p, scan.g++);
+        ti.kb_lo = min(scan.kb, p.num_kb);
+        ti.kb_hi = min(scan.kb + k_segment_blocks(p, g), p.num_kb);
+        ti.group = g;
+    }
     const int per_group = p.group_m * p.num_n_blocks;
     const int grp = t / per_group;
     const int rem = t - grp * per_group;
@@ -110,8 +127,9 @@ __device__ __forceinline__ PairTile get_pair_tile(const GemmParams &p, int t, in
         ti.b_row = g * p.n + ti.n_blk * PAIR_BN + half;
         ti.row_limit = min(BLOCK_M, cnt - row0);
     } else {
+        // dense, or K-grouped (A and B shared by the groups; the group picks
+        // the K range and the output plane)
         ti.valid = 1;
-        ti.group = 0;
         const int row0 = pb_lin * PAIR_ROWS + half;
         ti.a_row = row0;
         ti.sa_row = row0;
@@ -130,7 +148,10 @@ __global__ void __launch_bounds__(DEFER ? PAIR_DEFER_THREADS : NUM_THREADS, 1)
     fp8_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                          const __grid_constant__ CUtensorMap tmap_d, const __grid_constant__ CUtensorMap tmap_sa,
                          const GemmParams p) {
-    static_assert(KIND == KIND_DENSE || KIND == KIND_MASKED, "pair tiles: dense and masked layouts");
+    static_assert(KIND == KIND_DENSE || KIND == KIND_MASKED || KIND == KIND_KGROUPED,
+                  "pair tiles: dense, masked and K-grouped layouts");
+    // rows of D past the bound are clipped by the tensor map (no per-row stores)
+    constexpr bool CLIPPED = KIND == KIND_DENSE || KIND == KIND_KGROUPED;
     static_assert((SS & (SS - 1)) == 0, "scale ring size");
     static_assert(!(DEFER && F32OUT), "deferred stores: BF16 output");
     using L = PairSmemLayout<STAGES, SS, DEFER>;
@@ -217,9 +238,21 @@ __global__ void __launch_bounds__(DEFER ? PAIR_DEFER_THREADS : NUM_THREADS, 1)
             }
         }
     }
+    if constexpr (KIND == KIND_KGROUPED) {
+        // segment lengths: multiples of 128 that fit in K (others are reported)
+        if (blockIdx.x == 0 && warp == 0 && lane == 0) {
+            long long total = 0;
+            for (int g = 0; g < p.num_groups; ++g) {
+                const int c = __ldg(p.k_sizes + g);
+                if (c < 0 || c % BLOCK_K != 0) record_error(p, DEV_ERR_CHECK, (uint32_t)g);
+                total += c > 0 ? c : 0;
+            }
+            if (total > p.k) record_error(p, DEV_ERR_CHECK, (uint32_t)p.num_groups);
+        }
+    }
 
     const int pblocks = total_pair_blocks<KIND>(p);
-    const int num_tiles = pblocks * p.num_n_blocks;
+    const int num_tiles = pblocks * p.num_n_blocks * (KIND == KIND_KGROUPED ? p.num_groups : 1);
     const int t_begin = (int)(blockIdx.x >> 1), t_step = (int)(gridDim.x >> 1);
 
     if (warp == PRODUCER_WARP) {
@@ -227,18 +260,20 @@ __global__ void __launch_bounds__(DEFER ? PAIR_DEFER_THREADS : NUM_THREADS, 1)
         if (lane == 0) {
             uint32_t it = 0;
             bool ok = true;
+            KScan scan;
             for (int t = t_begin; t < num_tiles && ok; t += t_step) {
-                const PairTile ti = get_pair_tile<KIND>(p, t, pblocks, rank);
+                const PairTile ti = get_pair_tile<KIND>(p, t, pblocks, rank, scan);
                 if (!ti.valid) continue;
                 const int nb0 = min((ti.n_blk * BN) / 128, p.num_nb - 1);
                 const int nb1 = min((ti.n_blk * BN + BN / 2) / 128, p.num_nb - 1);
-                const float *sb0 = p.sB + ((size_t)ti.group * p.num_nb + nb0) * p.num_kb;
-                const float *sb1 = p.sB + ((size_t)ti.group * p.num_nb + nb1) * p.num_kb;
-                for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
+                const int bgroup = KIND == KIND_KGROUPED ? 0 : ti.group;  // K-grouped: one B for all groups
+                const float *sb0 = p.sB + ((size_t)bgroup * p.num_nb + nb0) * p.num_kb;
+                const float *sb1 = p.sB + ((size_t)bgroup * p.num_nb + nb1) * p.num_kb;
+                for (int kb = ti.kb_lo; kb < ti.kb_hi; ++kb, ++it) {
                     const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
                     const uint32_t q = it % SS, qph = (it / SS) & 1u;
-                    if (!wait_phase(empty_bar(s), ph ^ 1u, abort_flag, p, ROLE_PRODUCER) ||
-                        !wait_phase(sempty_bar(q), qph ^ 1u, abort_flag, p, ROLE_PRODUCER)) {
+                    if (!wait_phase_call(empty_bar(s), ph ^ 1u, abort_flag, p, ROLE_PRODUCER) ||
+                        !wait_phase_call(sempty_bar(q), qph ^ 1u, abort_flag, p, ROLE_PRODUCER)) {
                         ok = false;
                         break;
                     }
@@ -285,14 +320,15 @@ __global__ void __launch_bounds__(DEFER ? PAIR_DEFER_THREADS : NUM_THREADS, 1)
         if (leader && lane == 0) {
             uint32_t it = 0;
             bool ok = true;
+            KScan scan;
             for (int t = t_begin; t < num_tiles && ok; t += t_step) {
-                const PairTile ti = get_pair_tile<KIND>(p, t, pblocks, rank);
+                const PairTile ti = get_pair_tile<KIND>(p, t, pblocks, rank, scan);
                 if (!ti.valid) continue;
-                for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
+                for (int kb = ti.kb_lo; kb < ti.kb_hi; ++kb, ++it) {
                     const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
                     const uint32_t b = it & (NTB - 1u), bph = (it / NTB) & 1u;
-                    if (!wait_phase(tempty_bar(b), bph ^ 1u, abort_flag, p, ROLE_MMA) ||
-                        !wait_phase(full_bar(s), ph, abort_flag, p, ROLE_MMA)) {
+                    if (!wait_phase_call(tempty_bar(b), bph ^ 1u, abort_flag, p, ROLE_MMA) ||
+                        !wait_phase_call(full_bar(s), ph, abort_flag, p, ROLE_MMA)) {
                         ok = false;
                         break;
                     }
@@ -328,8 +364,9 @@ __global__ void __launch_bounds__(DEFER ? PAIR_DEFER_THREADS : NUM_THREADS, 1)
         uint32_t b = 0, bph = 0, q = 0, qph = 0;
         uint32_t ep = 0;  // DEFER: tiles staged so far (parity of the staging barriers)
         bool ok = true;
+        KScan scan;
         for (int t = t_begin; t < num_tiles && ok; t += t_step) {
-            const PairTile ti = get_pair_tile<KIND>(p, t, pblocks, rank);
+            const PairTile ti = get_pair_tile<KIND>(p, t, pblocks, rank, scan);
             if (!ti.valid) continue;
             const bool row_ok = r < ti.row_limit;
             const int col0 = ti.n_blk * BN + half * COLS;
@@ -338,9 +375,10 @@ __global__ void __launch_bounds__(DEFER ? PAIR_DEFER_THREADS : NUM_THREADS, 1)
 #pragma unroll
             for (int j = 0; j < COLS / 2; ++j) acc2[j] = 0ull;
 
-            for (int kb = 0; kb < p.num_kb; ++kb) {
-                const bool got = wait_phase(sfull_bar(q), qph, abort_flag, p, ROLE_EPILOGUE) &&
-                                 wait_phase(tfull_bar(b), bph, abort_flag, p, ROLE_EPILOGUE);
+            // (K-grouped: an empty segment leaves the sums at zero, and zeros are stored)
+            for (int kb = ti.kb_lo; kb < ti.kb_hi; ++kb) {
+                const bool got = wait_phase_call(sfull_bar(q), qph, abort_flag, p, ROLE_EPILOGUE) &&
+                                 wait_phase_call(tfull_bar(b), bph, abort_flag, p, ROLE_EPILOGUE);
                 if (!__all_sync(0xffffffffu, got)) {
                     ok = false;
                     break;
@@ -383,10 +421,12 @@ __global__ void __launch_bounds__(DEFER ? PAIR_DEFER_THREADS : NUM_THREADS, 1)
             float acc[COLS];
 #pragma unroll
             for (int j = 0; j < COLS / 2; ++j) unpack_f32x2(acc2[j], acc[2 * j], acc[2 * j + 1]);
+            // first row of this warp's block in D (K-grouped: within the group's
+            // output plane, the third coordinate of D's tensor map)
             const int d_row = ti.a_row + sub * 32;
             const bool rows_in = sub * 32 < ti.row_limit;  // some row of this warp is written
             bool use_tma;
-            if constexpr (KIND == KIND_DENSE)
+            if constexpr (CLIPPED)
                 use_tma = true;  // rows past m are clipped by the tensor map bounds
             else
                 use_tma = __all_sync(0xffffffffu, row_ok);
@@ -394,7 +434,7 @@ __global__ void __launch_bounds__(DEFER ? PAIR_DEFER_THREADS : NUM_THREADS, 1)
                 // the store warp has finished reading the previous tile's staging
                 // (every warp waits, so none can be a tile ahead of the others)
                 if (!__all_sync(0xffffffffu,
-                                wait_phase(stg_empty_bar, (ep & 1u) ^ 1u, abort_flag, p, ROLE_EPILOGUE)))
+                                wait_phase_call(stg_empty_bar, (ep & 1u) ^ 1u, abort_flag, p, ROLE_EPILOGUE)))
                     break;
                 ++ep;
             }
@@ -430,7 +470,10 @@ __global__ void __launch_bounds__(DEFER ? PAIR_DEFER_THREADS : NUM_THREADS, 1)
                         fence_proxy_async_smem();
                         __syncwarp();
                         if (lane == 0) {
-                            tma_store_2d(&tmap_d, stg, x, d_row);
+                            if constexpr (KIND == KIND_KGROUPED)
+                                tma_store_3d(&tmap_d, stg, x, d_row, ti.group);
+                            else
+                                tma_store_2d(&tmap_d, stg, x, d_row);
                             bulk_commit_group();
                         }
                     }
@@ -451,7 +494,10 @@ __global__ void __launch_bounds__(DEFER ? PAIR_DEFER_THREADS : NUM_THREADS, 1)
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) {
-                        tma_store_2d(&tmap_d, stg, x, d_row);
+                        if constexpr (KIND == KIND_KGROUPED)
+                            tma_store_3d(&tmap_d, stg, x, d_row, ti.group);
+                        else
+                            tma_store_2d(&tmap_d, stg, x, d_row);
                         bulk_commit_group();
                     }
                 }
@@ -498,22 +544,26 @@ __global__ void __launch_bounds__(DEFER ? PAIR_DEFER_THREADS : NUM_THREADS, 1)
         // it back.
         if (lane == 0) {
             uint32_t ep = 0;
+            KScan scan;
             for (int t = t_begin; t < num_tiles; t += t_step) {
-                const PairTile ti = get_pair_tile<KIND>(p, t, pblocks, rank);
+                const PairTile ti = get_pair_tile<KIND>(p, t, pblocks, rank, scan);
                 if (!ti.valid) continue;
-                if (!wait_phase(stg_full_bar, ep & 1u, abort_flag, p, ROLE_EPILOGUE)) break;
+                if (!wait_phase_call(stg_full_bar, ep & 1u, abort_flag, p, ROLE_EPILOGUE)) break;
                 ++ep;
                 for (int w = 0; w < NUM_EPI_WARPS; ++w) {
                     const int wsub = w & 3, whalf = w >> 2;
                     const bool rows_in = wsub * 32 < ti.row_limit;
-                    const bool all_rows = KIND == KIND_DENSE || wsub * 32 + 32 <= ti.row_limit;
+                    const bool all_rows = CLIPPED || wsub * 32 + 32 <= ti.row_limit;
                     if (!rows_in || !all_rows) continue;  // nothing staged, or stored row by row
                     const int d_row = ti.a_row + wsub * 32;
                     for (int bx = 0; bx < COLS / 64; ++bx) {
                         const int x = ti.n_blk * BN + whalf * COLS + bx * 64;
                         if (x >= p.n) continue;
-                        tma_store_2d(&tmap_d, sbase + L::STG_OFF + w * L::STG_PER_WARP + bx * STAGING_BYTES_PER_WARP,
-                                     x, d_row);
+                        const uint32_t src = sbase + L::STG_OFF + w * L::STG_PER_WARP + bx * STAGING_BYTES_PER_WARP;
+                        if constexpr (KIND == KIND_KGROUPED)
+                            tma_store_3d(&tmap_d, src, x, d_row, ti.group);
+                        else
+                            tma_store_2d(&tmap_d, src, x, d_row);
                     }
                 }
                 bulk_commit_group();

@@ -243,8 +243,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 for (int kb = kb_begin; kb < kb_end; ++kb, ++it) {
                     const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
                     const uint32_t q = it % SCALE_STAGES, qph = (it / SCALE_STAGES) & 1u;
-                    if (!wait_phase(empty_bar(s), ph ^ 1u, abort_flag, p, ROLE_PRODUCER) ||
-                        !wait_phase(sempty_bar(q), qph ^ 1u, abort_flag, p, ROLE_PRODUCER)) {
+                    if (!wait_phase_call(empty_bar(s), ph ^ 1u, abort_flag, p, ROLE_PRODUCER) ||
+                        !wait_phase_call(sempty_bar(q), qph ^ 1u, abort_flag, p, ROLE_PRODUCER)) {
                         ok = false;
                         break;
                     }
@@ -289,8 +289,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 for (int kb = kb_begin; kb < kb_end; ++kb, ++it) {
                     const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
                     const uint32_t b = it & (NTB - 1u), bph = (it / NTB) & 1u;
-                    if (!wait_phase(tempty_bar(b), bph ^ 1u, abort_flag, p, ROLE_MMA) ||
-                        !wait_phase(full_bar(s), ph, abort_flag, p, ROLE_MMA)) {
+                    if (!wait_phase_call(tempty_bar(b), bph ^ 1u, abort_flag, p, ROLE_MMA) ||
+                        !wait_phase_call(full_bar(s), ph, abort_flag, p, ROLE_MMA)) {
                         ok = false;
                         break;
                     }
@@ -331,8 +331,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             for (int j = 0; j < COLS / 2; ++j) acc2[j] = 0ull;
 
             for (int kb = kb_begin; kb < kb_end; ++kb) {
-                const bool got = wait_phase(sfull_bar(q), qph, abort_flag, p, ROLE_EPILOGUE) &&
-                                 wait_phase(tfull_bar(b), bph, abort_flag, p, ROLE_EPILOGUE);
+                const bool got = wait_phase_call(sfull_bar(q), qph, abort_flag, p, ROLE_EPILOGUE) &&
+                                 wait_phase_call(tfull_bar(b), bph, abort_flag, p, ROLE_EPILOGUE);
                 if (!__all_sync(0xffffffffu, got)) {
                     ok = false;
                     break;

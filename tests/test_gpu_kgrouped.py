@@ -46,6 +46,25 @@ def _compare_f32(got, ref64, what):
         assert float(np.linalg.norm(g - ref64)) / nr <= AGG_REL, what
 
 
+PLANS = ["auto", "one_cta_256", "cta_pair", "cta_pair_deferred"]
+
+
+@pytest.fixture(params=PLANS)
+def plan(request):
+    """The tile plans of the K-grouped call: the automatic choice, one-CTA
+    128 x 256 tiles, and 256 x 256 tiles on CTA pairs with the promotion
+    warps storing or with the store warp (forced even where M < 256)."""
+    name = request.param
+    if name != "auto":
+        fg.fg_set_config_override(256, 1)
+        fg.fg_set_pair_mode(0 if name == "one_cta_256" else 1)
+        fg.lib().fg_debug_set_pair_defer(1 if name == "cta_pair_deferred" else 0)
+    yield name
+    fg.fg_set_config_override(0, 0)
+    fg.fg_set_pair_mode(-1)
+    fg.lib().fg_debug_set_pair_defer(-1)
+
+
 @pytest.mark.parametrize("M,N,ks,K", [
     (200, 264, [128, 0, 256, 384], 896),      # ragged M and N, an empty group, 128 unused K columns
     (128, 256, [512], 512),
@@ -54,7 +73,7 @@ def _compare_f32(got, ref64, what):
     (257, 2112, [128] * 9, 1152),             # nine groups, the sweep's ragged N
 ])
 @pytest.mark.parametrize("f32", [False, True])
-def test_k_grouped_small_full(M, N, ks, K, f32):
+def test_k_grouped_small_full(M, N, ks, K, f32, plan):
     p = wl.k_grouped(M, N, ks, seed=M + N + K + len(ks), K=K)
     D = _run(p, ks, f32)
     ref16, ref64 = oracle.k_grouped(p.A, 0, p.sA, p.B, 0, p.sB, np.array(ks, np.int32))
@@ -94,7 +113,7 @@ def test_k_grouped_each_group_equals_dense_on_its_slice():
         fg.fg_set_config_override(0, 0)
 
 
-def test_k_grouped_graph_replay_reads_new_segment_lengths():
+def test_k_grouped_graph_replay_reads_new_segment_lengths(plan):
     """The lengths live on the device: a captured call replayed after they
     change gives the result of the new lengths."""
     p = wl.k_grouped(128, 256, [512], seed=73, K=512)
@@ -118,7 +137,7 @@ def test_k_grouped_graph_replay_reads_new_segment_lengths():
 
 
 @pytest.mark.parametrize("ks,detail", [([100, 128], 0), ([128, -128], 1), ([256, 384], 2)])
-def test_k_grouped_bad_segment_lengths_are_reported(ks, detail):
+def test_k_grouped_bad_segment_lengths_are_reported(ks, detail, plan):
     """A length that is not a multiple of 128, a negative one, or lengths that
     sum past K are recorded as FG_ERR_DEVICE_CHECK (detail: the group, or G for
     the sum); nothing faults and the next call is clean."""
@@ -149,3 +168,33 @@ def test_k_grouped_workload(G, M, N, tokens):
     cc = np.concatenate([pk[1] for pk in picks])
     ref16, _ = oracle.k_grouped_at(p.A, 0, p.sA, p.B, 0, p.sB, np.array(ks, np.int32), gs, rr, cc)
     compare(D[gs, rr, cc], ref16, what=f"k-grouped G={G} {M}x{N} (sampled)")
+
+
+@pytest.mark.parametrize("G,M,N,K,want", [
+    (4, 4096, 7168, 4 * 8192, (256, 1, 0, 0, 0)),    # segments of 64 K blocks: one-CTA tiles
+    (8, 4096, 2048, 8 * 1024, (256, 1, 1, 0, 1)),    # segments of 8: CTA pairs with the store warp
+    (2, 128, 512, 2 * 1024, (128, 1, 0, 0, 0)),      # a few one-CTA tiles: 128 wide
+    (8, 200, 4096, 8 * 512, (256, 1, 0, 0, 0)),      # fewer than 256 rows: one-CTA tiles
+    (32, 4096, 7168, 32 * 256, (256, 1, 1, 0, 0)),   # segments of 2 K blocks: pairs, promotion warps store
+])
+def test_k_grouped_plan_query(G, M, N, K, want):
+    got = fg.fg_query_plan(3, M, G, N, K)
+    assert tuple(got) == want, got
+
+
+def test_k_grouped_pair_tiles_workload_sampled():
+    """CTA-pair tiles with the store warp on a workload-shaped call whose
+    segments are short and ragged (an empty one among them), sampled outputs
+    of every plane, and the same call on one-CTA tiles agreeing within the
+    tolerance on the same samples."""
+    ks = [1024, 0, 384, 2048, 128, 896, 1536, 256]
+    M, N = 2304, 3072
+    p = wl.k_grouped(M, N, ks, seed=75)
+    assert fg.fg_query_plan(3, M, len(ks), N, p.k)[2:] == (1, 0, 1)
+    D = d_to_bits(_run(p, ks))
+    pk = sample_positions(M, N, seed=76, n_rows_full=2, boundary_tiles=True)
+    gs = np.repeat(np.arange(len(ks)), pk[0].size)
+    rr, cc = np.tile(pk[0], len(ks)), np.tile(pk[1], len(ks))
+    ref16, _ = oracle.k_grouped_at(p.A, 0, p.sA, p.B, 0, p.sB, np.array(ks, np.int32), gs, rr, cc)
+    compare(D[gs, rr, cc], ref16, what="k-grouped pair tiles (sampled)")
+    assert not np.any(D[1]), "empty segment must give zeros"
