@@ -32,7 +32,8 @@ STATUS_NAMES = {0: "FG_OK", 1: "FG_ERR_INVALID_ARG", 2: "FG_ERR_MISALIGNED", 3: 
                 4: "FG_ERR_CUDA", 5: "FG_ERR_TIMEOUT", 6: "FG_ERR_DEVICE_CHECK"}
 
 _lock = threading.Lock()
-_lib = None
+_libs = {}  # library path -> loaded handle
+_use_debug = False
 
 # exported symbols and their ctypes signatures (kept in step with include/fp8gemm.h)
 _P, _I, _U32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_uint32
@@ -62,6 +63,8 @@ SIGNATURES = {
     "fg_version": (_I, []),
     "fg_debug_skip_producer_iteration": (_I, [_I]),
     "fg_debug_set_pair_defer": (_I, [_I]),
+    "fg_debug_bad_coordinate": (_I, [_I]),
+    "fg_debug_build": (_I, []),
 }
 
 
@@ -71,23 +74,38 @@ class FGError(RuntimeError):
         super().__init__(f"{fn} failed: {STATUS_NAMES.get(status, status)}")
 
 
-def library_path() -> str:
-    return _build.LIB_PATH
+def library_path(debug: bool = False) -> str:
+    return _build.DEBUG_LIB_PATH if debug else _build.LIB_PATH
 
 
-def lib():
-    """The loaded C library (built in-tree on first use if missing)."""
-    global _lib
+def lib(debug=None):
+    """The loaded C library (built in-tree on first use if missing): the one
+    `use_debug_library` selected, or the one `debug` names."""
     with _lock:
-        if _lib is None:
-            path = _build.build() if os.environ.get("FG_NO_AUTOBUILD") != "1" else _build.LIB_PATH
+        dbg = _use_debug if debug is None else bool(debug)
+        path = library_path(dbg)
+        h = _libs.get(path)
+        if h is None:
+            if os.environ.get("FG_NO_AUTOBUILD") != "1":
+                _build.build(debug=dbg)
             h = ctypes.CDLL(path)
             for name, (res, args) in SIGNATURES.items():
                 f = getattr(h, name)
                 f.restype = res
                 f.argtypes = args
-            _lib = h
-        return _lib
+            _libs[path] = h
+        return h
+
+
+def use_debug_library(on: bool) -> None:
+    """Route later calls of this module to the debug build (libfp8gemm_debug.so:
+    FG_DEBUG device-side checks of every TMA box, ring index and TMEM column,
+    single-stage pipelines) or back to the library.  Process-wide; the two
+    libraries keep separate knobs and status words.  For bisecting a
+    suspected race or an out-of-bounds access, not for speed."""
+    global _use_debug
+    with _lock:
+        _use_debug = bool(on)
 
 
 def _check(name, st):

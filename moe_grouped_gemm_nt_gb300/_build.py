@@ -1,9 +1,13 @@
-"""Build the in-tree CUDA library libfp8gemm.so for sm_103a with nvcc.
+"""Build the in-tree CUDA libraries for sm_103a with nvcc.
 
-The library is a plain C ABI shared object (include/fp8gemm.h); the CUDA
-runtime is linked statically, so loading it needs no GPU driver, and the
-driver's tensor-map encoder is resolved at run time.  The translation units
-compile in parallel (one nvcc process each) and are linked into one object.
+libfp8gemm.so is the library; libfp8gemm_debug.so is the same sources compiled
+with FG_DEBUG: device-side checks of every TMA box, ring index and TMEM column
+(a failed check records FG_ERR_DEVICE_CHECK and skips the access) and the
+shallowest pipelines (one operand stage), for bisecting a race.  Both are plain
+C ABI shared objects (include/fp8gemm.h); the CUDA runtime is linked
+statically, so loading one needs no GPU driver, and the driver's tensor-map
+encoder is resolved at run time.  All translation units compile in parallel
+(one nvcc process each) and each library is linked into one object.
 """
 from __future__ import annotations
 
@@ -15,6 +19,8 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(BUILD_DIR, "libfp8gemm.so")
+DEBUG_LIB_PATH = os.path.join(BUILD_DIR, "libfp8gemm_debug.so")
+VARIANTS = {LIB_PATH: [], DEBUG_LIB_PATH: ["-DFG_DEBUG"]}
 SOURCES = ["fp8gemm.cu", "swap.cu"]
 HEADERS = ["gemm_kernel.cuh", "gemm_pair_kernel.cuh", "gemm_swap_kernel.cuh", "quantize_kernel.cuh", "ptx.cuh",
            "host_common.cuh", "swap.h"]
@@ -29,42 +35,64 @@ def nvcc() -> str:
     return "nvcc"
 
 
-def _stale() -> bool:
-    if not os.path.exists(LIB_PATH):
+def _stale(lib_path: str) -> bool:
+    if not os.path.exists(lib_path):
         return True
-    t = os.path.getmtime(LIB_PATH)
+    t = os.path.getmtime(lib_path)
     deps = [os.path.join(CSRC, f) for f in SOURCES + HEADERS]
     deps.append(os.path.join(ROOT, "include", "fp8gemm.h"))
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    """Compile the library if a source is newer than it; return its path."""
-    if not force and not _stale():
-        return LIB_PATH
+def _build(lib_paths, force: bool, verbose: bool) -> None:
+    todo = [p for p in lib_paths if force or _stale(p)]
+    if not todo:
+        return
     os.makedirs(BUILD_DIR, exist_ok=True)
     tag = f"tmp{os.getpid()}"
-    objs, procs = [], []
-    for src in SOURCES:
-        obj = os.path.join(BUILD_DIR, f"{os.path.splitext(src)[0]}.{tag}.o")
-        cmd = [nvcc(), *COMMON_FLAGS, "-I", os.path.join(ROOT, "include"), "-c", os.path.join(CSRC, src), "-o", obj]
-        if verbose:
-            cmd.insert(1, "-Xptxas=-v")
-        procs.append(subprocess.Popen(cmd))
-        objs.append(obj)
-    failed = [p.args for p in procs if p.wait() != 0]
+    jobs = []  # (library, objects, processes)
+    for lib_path in todo:
+        stem = os.path.splitext(os.path.basename(lib_path))[0]
+        objs, procs = [], []
+        for src in SOURCES:
+            obj = os.path.join(BUILD_DIR, f"{stem}.{os.path.splitext(src)[0]}.{tag}.o")
+            cmd = [nvcc(), *COMMON_FLAGS, *VARIANTS[lib_path], "-I", os.path.join(ROOT, "include"), "-c",
+                   os.path.join(CSRC, src), "-o", obj]
+            if verbose:
+                cmd.insert(1, "-Xptxas=-v")
+            procs.append(subprocess.Popen(cmd))
+            objs.append(obj)
+        jobs.append((lib_path, objs, procs))
     try:
+        failed = [p.args for _, _, procs in jobs for p in procs if p.wait() != 0]
         if failed:
             raise subprocess.CalledProcessError(1, failed[0])
-        tmp = LIB_PATH + f".{tag}"
-        subprocess.run([nvcc(), *ARCH_FLAGS, "-shared", "-cudart", "static", *objs, "-o", tmp], check=True)
-        os.replace(tmp, LIB_PATH)
+        for lib_path, objs, _ in jobs:
+            tmp = lib_path + f".{tag}"
+            subprocess.run([nvcc(), *ARCH_FLAGS, "-shared", "-cudart", "static", *objs, "-o", tmp], check=True)
+            os.replace(tmp, lib_path)
     finally:
-        for o in objs:
-            if os.path.exists(o):
-                os.remove(o)
-    return LIB_PATH
+        for _, objs, procs in jobs:
+            for p in procs:
+                p.wait()
+            for o in objs:
+                if os.path.exists(o):
+                    os.remove(o)
+
+
+def build(force: bool = False, verbose: bool = False, debug: bool = False) -> str:
+    """Compile the library (debug: the FG_DEBUG build) if a source is newer
+    than it; return its path."""
+    path = DEBUG_LIB_PATH if debug else LIB_PATH
+    _build([path], force, verbose)
+    return path
+
+
+def build_all(force: bool = False, verbose: bool = False) -> None:
+    """Compile both libraries, all translation units in parallel."""
+    _build(list(VARIANTS), force, verbose)
 
 
 if __name__ == "__main__":
-    print(build(force=True, verbose=True))
+    build_all(force=True, verbose=True)
+    print(LIB_PATH, DEBUG_LIB_PATH)

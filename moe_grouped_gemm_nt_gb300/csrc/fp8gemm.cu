@@ -34,6 +34,7 @@ std::atomic<int> g_pdl{1};
 std::atomic<int> g_force_split{0};
 std::atomic<int> g_pair_mode{-1};
 std::atomic<int> g_swap_mode{-1};
+std::atomic<int> g_debug_bad_coord{-1};
 
 DeviceInfo g_dev[kMaxDevices];
 std::mutex g_dev_mutex;
@@ -64,20 +65,32 @@ namespace {
 
 using namespace fgh;
 
-template <int BN, int STAGES, int KIND, bool SPLITK, bool F32OUT = false>
-using Kernel =
-    Launcher<fg::fp8_gemm_kernel<BN, STAGES, KIND, SPLITK, F32OUT>, fg::SmemLayout<BN, STAGES>::BYTES, SPLITK>;
+// Operand stages of the one-CTA kernel: 4 of 16 + 32 KB for 256-wide tiles, 6
+// of 16 + 16 KB for 128-wide ones (what fits beside the staging buffers).  The
+// debug build (FG_DEBUG) runs every pipeline on as few stages as it can: one,
+// or for split-K the fewest whose ring holds the FP32 partial tile (3 and 2),
+// so that a result which changes with the pipeline depth points at a missing
+// wait (the single-buffer bisection of the pages' debugging method).
+template <int BN, bool SPLITK>
+constexpr int one_cta_stages() {
+    if (fg::kDebugBuild) return SPLITK ? (BN == 256 ? 3 : 2) : 1;
+    return BN == 256 ? 4 : 6;
+}
+
+template <int BN, int KIND, bool SPLITK, bool F32OUT = false>
+using Kernel = Launcher<fg::fp8_gemm_kernel<BN, one_cta_stages<BN, SPLITK>(), KIND, SPLITK, F32OUT>,
+                        fg::SmemLayout<BN, one_cta_stages<BN, SPLITK>()>::BYTES, SPLITK>;
 
 // 256 x 256 tiles on CTA pairs: operand stages of 16 + 16 KB per CTA, and a
 // scale ring at least as deep (the producer issues both in the same iteration)
-constexpr int kPairStages = 5;
+constexpr int kPairStages = fg::kDebugBuild ? 1 : 5;
 constexpr int kPairScaleStages = 8;
 template <int KIND, bool F32OUT = false>
 using PairKernel = Launcher<fg::fp8_gemm_pair_kernel<KIND, kPairStages, kPairScaleStages, F32OUT>,
                             fg::PairSmemLayout<kPairStages, kPairScaleStages>::BYTES, true>;
 // deferred stores (BF16 output): the staging holds a whole tile, bought with
 // one operand stage less
-constexpr int kPairDeferStages = 4;
+constexpr int kPairDeferStages = fg::kDebugBuild ? 1 : 4;
 template <int KIND>
 using PairDeferKernel = Launcher<fg::fp8_gemm_pair_kernel<KIND, kPairDeferStages, kPairScaleStages, false, true>,
                                  fg::PairSmemLayout<kPairDeferStages, kPairScaleStages, true>::BYTES, true,
@@ -146,8 +159,8 @@ Plan choose_plan(long long m_blocks, int rows, int n, int k, int sms) {
             if (sp > 1 && num_kb < 2 * sp) break;  // at least two K blocks per rank
             long long cap = sms;
             if (sp > 1) {
-                const int clusters = bn == 256 ? Kernel<256, 4, fg::KIND_DENSE, true>::max_active_clusters(sp)
-                                               : Kernel<128, 6, fg::KIND_DENSE, true>::max_active_clusters(sp);
+                const int clusters = bn == 256 ? Kernel<256, fg::KIND_DENSE, true>::max_active_clusters(sp)
+                                               : Kernel<128, fg::KIND_DENSE, true>::max_active_clusters(sp);
                 cap = (long long)sp * clusters;
                 if (cap > (long long)(sms / sp) * sp) cap = (long long)(sms / sp) * sp;  // the SM limit
                 // a second wave of clusters would pay start-up and exchange again
@@ -268,6 +281,9 @@ fg_status run(const void *A, int a_fmt, const float *sA, int ld_sA, const void *
     p.status = dev->status;
     p.timeout_ns = (unsigned long long)g_watchdog_ms.load() * 1000000ull;
     p.debug_skip_iter = g_debug_skip_iter.exchange(-1);
+    p.a_rows_total = (int)a_rows_total;
+    p.b_rows_total = G * n;
+    p.debug_bad_coord = g_debug_bad_coord.exchange(-1);
 
     if constexpr (KIND != fg::KIND_CONTIGUOUS) {
         if (pair) {
@@ -298,17 +314,17 @@ fg_status run(const void *A, int a_fmt, const float *sA, int ld_sA, const void *
             const long long grid = max_tiles * plan.split;
             if (grid > INT32_MAX) return FG_ERR_UNSUPPORTED;
             if (BN == 256)
-                return Kernel<256, 4, KIND, true, F32OUT>::launch(ta, tb, td, tsa, p, (int)grid, plan.split,
+                return Kernel<256, KIND, true, F32OUT>::launch(ta, tb, td, tsa, p, (int)grid, plan.split,
                                                                   stream);
-            return Kernel<128, 6, KIND, true, F32OUT>::launch(ta, tb, td, tsa, p, (int)grid, plan.split, stream);
+            return Kernel<128, KIND, true, F32OUT>::launch(ta, tb, td, tsa, p, (int)grid, plan.split, stream);
         }
         if (BN == 128) {
             const int grid = (int)(max_tiles < sms ? max_tiles : sms);
-            return Kernel<128, 6, KIND, false, F32OUT>::launch(ta, tb, td, tsa, p, grid, 1, stream);
+            return Kernel<128, KIND, false, F32OUT>::launch(ta, tb, td, tsa, p, grid, 1, stream);
         }
     }
     const int grid = (int)(max_tiles < sms ? max_tiles : sms);
-    return Kernel<256, 4, KIND, false, F32OUT>::launch(ta, tb, td, tsa, p, grid, 1, stream);
+    return Kernel<256, KIND, false, F32OUT>::launch(ta, tb, td, tsa, p, grid, 1, stream);
 }
 
 // K-grouped entry points: G groups, each an NT product over its own segment of
@@ -404,6 +420,9 @@ fg_status run_kgrouped(const void *A, int a_fmt, const float *sA, int ld_sA, con
     p.status = dev->status;
     p.timeout_ns = (unsigned long long)g_watchdog_ms.load() * 1000000ull;
     p.debug_skip_iter = g_debug_skip_iter.exchange(-1);
+    p.a_rows_total = M;
+    p.b_rows_total = N;
+    p.debug_bad_coord = g_debug_bad_coord.exchange(-1);
     if (pair) {
         // the raster counts 256-row blocks within each group's plane
         const int pblocks = cdiv(M, fg::PAIR_ROWS);
@@ -426,8 +445,8 @@ fg_status run_kgrouped(const void *A, int a_fmt, const float *sA, int ld_sA, con
     const long long tiles = (long long)G * p.num_m_blocks * p.num_n_blocks;
     const int grid = (int)(tiles < sms ? tiles : sms);
     if (BN == 128)
-        return Kernel<128, 6, fg::KIND_KGROUPED, false, F32OUT>::launch(ta, tb, td, tsa, p, grid, 1, stream);
-    return Kernel<256, 4, fg::KIND_KGROUPED, false, F32OUT>::launch(ta, tb, td, tsa, p, grid, 1, stream);
+        return Kernel<128, fg::KIND_KGROUPED, false, F32OUT>::launch(ta, tb, td, tsa, p, grid, 1, stream);
+    return Kernel<256, fg::KIND_KGROUPED, false, F32OUT>::launch(ta, tb, td, tsa, p, grid, 1, stream);
 }
 
 }  // namespace
@@ -699,6 +718,20 @@ fg_status fg_set_watchdog_ms(uint32_t ms) {
     g_watchdog_ms.store(ms == 0 ? kDefaultWatchdogMs : ms);
     return FG_OK;
 }
+
+// Test hook of the debug build (not part of the public header): in the next
+// GEMM call, the producer of every CTA moves the A load of its K iteration
+// `iter` past K; the debug build's bounds check catches it before the load is
+// issued (records FG_ERR_DEVICE_CHECK, tag 0x41).  The release build ignores
+// the hook (FG_ERR_UNSUPPORTED).
+fg_status fg_debug_bad_coordinate(int iter) {
+    if (!fg::kDebugBuild) return FG_ERR_UNSUPPORTED;
+    g_debug_bad_coord.store(iter);
+    return FG_OK;
+}
+
+// Whether this library is the debug build (FG_DEBUG): 1 or 0.
+int fg_debug_build(void) { return fg::kDebugBuild ? 1 : 0; }
 
 // Test hook (not part of the public header): in the next GEMM call, the
 // producer of every CTA leaves its K iteration `iter` unarmed, so the MMA

@@ -98,6 +98,10 @@ struct GemmParams {
     uint32_t *status;  // [0] first error code, [1] its detail
     unsigned long long timeout_ns;
     int debug_skip_iter;  // producer leaves this K iteration unarmed (-1: never)
+    // extents of the tensor maps' row spaces, for the debug build's checks
+    int a_rows_total;     // rows of A and (2-D maps) of D: dense m, contiguous M, masked G * M_cap, K-grouped M
+    int b_rows_total;     // rows of B: G * n (K-grouped: N)
+    int debug_bad_coord;  // debug build: the A load of this K iteration is sent past K (-1: never)
 };
 
 template <int BN, int STAGES>
@@ -118,13 +122,67 @@ struct SmemLayout {
     static constexpr int BYTES = MISC_OFF + 16;
     // split-K partial tile (128 x BN FP32), aliased on the operand ring
     static constexpr int P_OFF = 0;
-    static_assert(BLOCK_M * BN * 4 <= STG_OFF, "partial tile must fit in the operand ring");
+    static constexpr bool PARTIAL_FITS = BLOCK_M * BN * 4 <= STG_OFF;
 };
 
 __device__ __forceinline__ int clamp_count(int c, int cap) { return c < 0 ? 0 : (c > cap ? cap : c); }
 
 __device__ __forceinline__ void record_error(const GemmParams &p, uint32_t code, uint32_t detail) {
     if (atomicCAS(p.status, 0u, code) == 0u) atomicExch(p.status + 1, detail);
+}
+
+// Debug build (compiled with FG_DEBUG): every TMA box start, ring index and
+// TMEM column is checked against what the launch allows before it is used.
+// A failed check records FG_ERR_DEVICE_CHECK with a tag in bits 24..31 of the
+// detail (the offending value in bits 0..23), raises the CTA's abort flag and
+// skips the access; the other roles then leave through their bounded waits.
+// The promotion warps also flag a non-finite K-block partial (finite inputs
+// never give one).  In the release build the checks compile to nothing.
+#ifdef FG_DEBUG
+constexpr bool kDebugBuild = true;
+#else
+constexpr bool kDebugBuild = false;
+#endif
+enum : uint32_t {
+    DBG_TMA_A = 0x41,  // A (or LHS scale) box start
+    DBG_TMA_B = 0x42,  // B box start
+    DBG_TMA_D = 0x43,  // D store box start
+    DBG_RING = 0x44,   // operand / scale ring slot or TMEM buffer index
+    DBG_TMEM = 0x45,   // TMEM column range of a load or an MMA
+    DBG_NONFINITE = 0x46,  // a K-block partial holds Inf or NaN (detail: the K block)
+};
+
+__device__ __forceinline__ bool dbg_ok(const GemmParams &p, bool ok, uint32_t tag, int value) {
+    if constexpr (kDebugBuild) {
+        if (!ok) {
+            record_error(p, DEV_ERR_CHECK, (tag << 24) | ((uint32_t)value & 0xFFFFFFu));
+            return false;
+        }
+    }
+    return true;
+}
+
+// A box starting at (x, y) in [0, x_end) x [0, y_end).  Stores pass the row
+// extent; loads pass load_row_limit() of it: a load box may start up to one
+// 256-row tile past the end (the missing rows of a partial tile are loaded as
+// zeros, never stored).
+__device__ __forceinline__ bool dbg_box(const GemmParams &p, int x, int x_end, int y, int y_end, uint32_t tag) {
+    return dbg_ok(p, x >= 0 && x < x_end, tag, x) && dbg_ok(p, y >= 0 && y < y_end, tag, y);
+}
+
+__device__ __forceinline__ int load_row_limit(int rows) { return rows + 256; }
+
+// TMA store of one staged box of D at column x, row d_row (K-grouped: of the
+// group's output plane, the map's third coordinate).
+template <int KIND>
+__device__ __forceinline__ void store_d_box(const CUtensorMap *map, uint32_t src, int x, int d_row, int group,
+                                            const GemmParams &p) {
+    if constexpr (KIND == KIND_KGROUPED) {
+        if (dbg_box(p, x, p.n, d_row, p.rows, DBG_TMA_D) && dbg_ok(p, group < p.num_groups, DBG_TMA_D, group))
+            tma_store_3d(map, src, x, d_row, group);
+    } else {
+        if (dbg_box(p, x, p.n, d_row, p.a_rows_total, DBG_TMA_D)) tma_store_2d(map, src, x, d_row);
+    }
 }
 
 struct Tile {
@@ -313,6 +371,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     const GemmParams p) {
     static_assert(BN == 128 || BN == 256, "BN must be 128 or 256");
     using L = SmemLayout<BN, STAGES>;
+    static_assert(!SPLITK || L::PARTIAL_FITS, "split-K: the partial tile must fit in the operand ring");
     constexpr int COLS = BN / 2;  // columns per promotion warp
     constexpr uint32_t STAGE_TX = A_STAGE_BYTES + L::B_STAGE_BYTES;
     constexpr uint32_t NTB = L::NUM_TBUF;  // TMEM accumulator buffers (a power of two)
@@ -448,9 +507,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         break;
                     }
                     if ((int)it == p.debug_skip_iter) continue;
+                    int ax = kb * BLOCK_K;
+                    if constexpr (kDebugBuild) {
+                        if ((int)it == p.debug_bad_coord) ax += p.num_kb * BLOCK_K;
+                        const int sa_rows = KIND == KIND_MASKED ? p.rows : p.a_rows_total;
+                        const int sa_row = KIND == KIND_MASKED ? ti.m_blk * BLOCK_M : ti.a_row;
+                        if (!(dbg_ok(p, s < (uint32_t)STAGES && q < (uint32_t)SCALE_STAGES, DBG_RING, (int)it) &&
+                              dbg_box(p, ax, p.k, ti.a_row, load_row_limit(p.a_rows_total), DBG_TMA_A) &&
+                              dbg_box(p, kb * BLOCK_K, p.k, ti.b_row, load_row_limit(p.b_rows_total), DBG_TMA_B) &&
+                              dbg_box(p, kb, p.num_kb, sa_row, load_row_limit(sa_rows), DBG_TMA_A) &&
+                              dbg_ok(p, ti.group >= 0 && ti.group < p.num_groups, DBG_TMA_B, ti.group))) {
+                            *abort_flag = 1u;
+                            ok = false;
+                            break;
+                        }
+                    }
                     mbar_arrive_expect_tx(full_bar(s), STAGE_TX);
-                    tma_load_2d(sbase + L::A_OFF + s * A_STAGE_BYTES, &tmap_a, full_bar(s), kb * BLOCK_K,
-                                ti.a_row);
+                    tma_load_2d(sbase + L::A_OFF + s * A_STAGE_BYTES, &tmap_a, full_bar(s), ax, ti.a_row);
                     tma_load_2d(sbase + L::B_OFF + s * L::B_STAGE_BYTES, &tmap_b, full_bar(s), kb * BLOCK_K,
                                 ti.b_row);
                     mbar_arrive_expect_tx(sfull_bar(q), SA_STAGE_BYTES);
@@ -496,6 +569,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         !wait_phase(full_bar(s), ph, abort_flag, p, ROLE_MMA)) {
                         ok = false;
                         break;
+                    }
+                    if constexpr (kDebugBuild) {
+                        if (!dbg_ok(p, s < (uint32_t)STAGES && b < NTB && (b + 1) * BN <= L::TMEM_COLS, DBG_TMEM,
+                                    (int)it)) {
+                            *abort_flag = 1u;
+                            ok = false;
+                            break;
+                        }
                     }
                     tc_fence_after();
                     const uint64_t adesc = make_desc_kmajor_sw128(sbase + L::A_OFF + s * A_STAGE_BYTES);
@@ -575,6 +656,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     ok = false;
                     break;
                 }
+                if constexpr (kDebugBuild) {
+                    const bool in = dbg_ok(p,
+                                           b < NTB && q < (uint32_t)SCALE_STAGES &&
+                                               (int)b * BN + half * COLS + COLS <= L::TMEM_COLS,
+                                           DBG_TMEM, kb);
+                    if (!__all_sync(0xffffffffu, in)) {
+                        *abort_flag = 1u;
+                        ok = false;
+                        break;
+                    }
+                }
                 tc_fence_after();
                 const float sc = ld_shared_f32(sa_addr + q * SA_STAGE_BYTES) *
                                  ld_shared_f32(sb_addr + q * SB_STAGE_BYTES);
@@ -591,6 +683,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     tmem_ld_wait();
 #pragma unroll
                     for (int j = 0; j < TMEM_LD_COLS; ++j) reg_fence(v[j]);
+                    if constexpr (kDebugBuild) {
+                        bool fin = true;
+#pragma unroll
+                        for (int j = 0; j < TMEM_LD_COLS; ++j) fin = fin && isfinite(__uint_as_float(v[j]));
+                        dbg_ok(p, fin, DBG_NONFINITE, kb);
+                    }
                     if (c == COLS / TMEM_LD_COLS - 1) {
                         // all of this K block's partial is in registers: hand the
                         // TMEM buffer back to the MMA warp before the last FMAs
@@ -661,10 +759,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         fence_proxy_async_smem();
                         __syncwarp();
                         if (lane == 0) {
-                            if constexpr (KIND == KIND_KGROUPED)
-                                tma_store_3d(&tmap_d, stg, x, d_row, ti.group);
-                            else
-                                tma_store_2d(&tmap_d, stg, x, d_row);
+                            store_d_box<KIND>(&tmap_d, stg, x, d_row, ti.group, p);
                             bulk_commit_group();
                         }
                     }
@@ -685,10 +780,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) {
-                        if constexpr (KIND == KIND_KGROUPED)
-                            tma_store_3d(&tmap_d, stg, x, d_row, ti.group);
-                        else
-                            tma_store_2d(&tmap_d, stg, x, d_row);
+                        store_d_box<KIND>(&tmap_d, stg, x, d_row, ti.group, p);
                         bulk_commit_group();
                     }
                 }

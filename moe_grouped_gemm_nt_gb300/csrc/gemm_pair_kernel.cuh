@@ -278,10 +278,23 @@ __global__ void __launch_bounds__(DEFER ? PAIR_DEFER_THREADS : NUM_THREADS, 1)
                         break;
                     }
                     if ((int)it == p.debug_skip_iter) continue;
+                    int ax = kb * BLOCK_K;
+                    if constexpr (kDebugBuild) {
+                        if ((int)it == p.debug_bad_coord) ax += p.num_kb * BLOCK_K;
+                        const int sa_rows = KIND == KIND_MASKED ? p.rows : p.a_rows_total;
+                        if (!(dbg_ok(p, s < (uint32_t)STAGES && q < (uint32_t)SS, DBG_RING, (int)it) &&
+                              dbg_box(p, ax, p.k, ti.a_row, load_row_limit(p.a_rows_total), DBG_TMA_A) &&
+                              dbg_box(p, kb * BLOCK_K, p.k, ti.b_row, load_row_limit(p.b_rows_total), DBG_TMA_B) &&
+                              dbg_box(p, kb, p.num_kb, ti.sa_row, load_row_limit(sa_rows), DBG_TMA_A) &&
+                              dbg_ok(p, ti.group >= 0 && ti.group < p.num_groups, DBG_TMA_B, ti.group))) {
+                            *abort_flag = 1u;
+                            ok = false;
+                            break;
+                        }
+                    }
                     if (leader) mbar_arrive_expect_tx(full_bar(s), PAIR_TX);
                     const uint32_t lead_full = map_shared_rank(full_bar(s), 0);
-                    tma_load_2d_pair(sbase + L::A_OFF + s * A_STAGE_BYTES, &tmap_a, lead_full, kb * BLOCK_K,
-                                     ti.a_row);
+                    tma_load_2d_pair(sbase + L::A_OFF + s * A_STAGE_BYTES, &tmap_a, lead_full, ax, ti.a_row);
                     tma_load_2d_pair(sbase + L::B_OFF + s * L::HB_STAGE_BYTES, &tmap_b, lead_full, kb * BLOCK_K,
                                      ti.b_row);
                     mbar_arrive_expect_tx(sfull_bar(q), SA_STAGE_BYTES);
@@ -331,6 +344,14 @@ __global__ void __launch_bounds__(DEFER ? PAIR_DEFER_THREADS : NUM_THREADS, 1)
                         !wait_phase_call(full_bar(s), ph, abort_flag, p, ROLE_MMA)) {
                         ok = false;
                         break;
+                    }
+                    if constexpr (kDebugBuild) {
+                        if (!dbg_ok(p, s < (uint32_t)STAGES && b < NTB && (int)(b + 1) * BN <= L::TMEM_COLS, DBG_TMEM,
+                                    (int)it)) {
+                            *abort_flag = 1u;
+                            ok = false;
+                            break;
+                        }
                     }
                     tc_fence_after();
                     const uint64_t adesc = make_desc_kmajor_sw128(sbase + L::A_OFF + s * A_STAGE_BYTES);
@@ -383,6 +404,17 @@ __global__ void __launch_bounds__(DEFER ? PAIR_DEFER_THREADS : NUM_THREADS, 1)
                     ok = false;
                     break;
                 }
+                if constexpr (kDebugBuild) {
+                    const bool in = dbg_ok(p,
+                                           b < NTB && q < (uint32_t)SS &&
+                                               (int)b * BN + half * COLS + COLS <= L::TMEM_COLS,
+                                           DBG_TMEM, kb);
+                    if (!__all_sync(0xffffffffu, in)) {
+                        *abort_flag = 1u;
+                        ok = false;
+                        break;
+                    }
+                }
                 tc_fence_after();
                 const float sc = ld_shared_f32(sa_addr + q * SA_STAGE_BYTES) *
                                  ld_shared_f32(sb_addr + q * SB_STAGE_BYTES);
@@ -399,6 +431,12 @@ __global__ void __launch_bounds__(DEFER ? PAIR_DEFER_THREADS : NUM_THREADS, 1)
                     tmem_ld_wait();
 #pragma unroll
                     for (int j = 0; j < TMEM_LD_COLS; ++j) reg_fence(v[j]);
+                    if constexpr (kDebugBuild) {
+                        bool fin = true;
+#pragma unroll
+                        for (int j = 0; j < TMEM_LD_COLS; ++j) fin = fin && isfinite(__uint_as_float(v[j]));
+                        dbg_ok(p, fin, DBG_NONFINITE, kb);
+                    }
                     if (c == COLS / TMEM_LD_COLS - 1) {
                         // the partial is in registers: hand the buffer back to the
                         // even CTA's MMA warp before the last FMAs
@@ -470,10 +508,7 @@ __global__ void __launch_bounds__(DEFER ? PAIR_DEFER_THREADS : NUM_THREADS, 1)
                         fence_proxy_async_smem();
                         __syncwarp();
                         if (lane == 0) {
-                            if constexpr (KIND == KIND_KGROUPED)
-                                tma_store_3d(&tmap_d, stg, x, d_row, ti.group);
-                            else
-                                tma_store_2d(&tmap_d, stg, x, d_row);
+                            store_d_box<KIND>(&tmap_d, stg, x, d_row, ti.group, p);
                             bulk_commit_group();
                         }
                     }
@@ -494,10 +529,7 @@ __global__ void __launch_bounds__(DEFER ? PAIR_DEFER_THREADS : NUM_THREADS, 1)
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) {
-                        if constexpr (KIND == KIND_KGROUPED)
-                            tma_store_3d(&tmap_d, stg, x, d_row, ti.group);
-                        else
-                            tma_store_2d(&tmap_d, stg, x, d_row);
+                        store_d_box<KIND>(&tmap_d, stg, x, d_row, ti.group, p);
                         bulk_commit_group();
                     }
                 }
@@ -559,11 +591,9 @@ __global__ void __launch_bounds__(DEFER ? PAIR_DEFER_THREADS : NUM_THREADS, 1)
                     for (int bx = 0; bx < COLS / 64; ++bx) {
                         const int x = ti.n_blk * BN + whalf * COLS + bx * 64;
                         if (x >= p.n) continue;
-                        const uint32_t src = sbase + L::STG_OFF + w * L::STG_PER_WARP + bx * STAGING_BYTES_PER_WARP;
-                        if constexpr (KIND == KIND_KGROUPED)
-                            tma_store_3d(&tmap_d, src, x, d_row, ti.group);
-                        else
-                            tma_store_2d(&tmap_d, src, x, d_row);
+                        store_d_box<KIND>(&tmap_d,
+                                          sbase + L::STG_OFF + w * L::STG_PER_WARP + bx * STAGING_BYTES_PER_WARP, x,
+                                          d_row, ti.group, p);
                     }
                 }
                 bulk_commit_group();

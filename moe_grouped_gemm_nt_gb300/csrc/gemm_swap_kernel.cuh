@@ -55,7 +55,7 @@ struct SwapSmemLayout {
     static constexpr int BYTES = MISC_OFF + 16;
     // split-K partial (128 weight rows x BT tokens, FP32), aliased on the operand ring
     static constexpr int P_OFF = 0;
-    static_assert(BLOCK_M * BT * 4 <= STG_OFF, "partial tile must fit in the operand ring");
+    static constexpr bool PARTIAL_FITS = BLOCK_M * BT * 4 <= STG_OFF;
 };
 
 struct SwapTile {
@@ -145,6 +145,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     static_assert(BT == 128 || BT == 256, "token tile of 128 or 256");
     static_assert(KIND == KIND_DENSE || KIND == KIND_MASKED, "swap-AB: dense and masked layouts");
     using L = SwapSmemLayout<BT, STAGES>;
+    static_assert(!SPLITK || L::PARTIAL_FITS, "split-K: the partial tile must fit in the operand ring");
     constexpr int COLS = BT / 2;  // token columns per promotion warp
     constexpr uint32_t STAGE_TX = L::W_STAGE_BYTES + L::T_STAGE_BYTES;
     constexpr uint32_t NTB = L::NUM_TBUF;

@@ -12,15 +12,17 @@ namespace {
 
 // Operand stages: 6 of 16 + 16 KB for 128-token tiles, 3 of 16 + 32 KB for
 // 256-token tiles (with the staging buffers and the 4-deep scale ring, the
-// most that fits in 227 KB of shared memory).
-template <int BT>
+// most that fits in 227 KB of shared memory).  The debug build: one stage, or
+// for split-K the fewest that hold the FP32 partial tile.
+template <int BT, bool SPLITK>
 constexpr int swap_stages() {
+    if (fg::kDebugBuild) return SPLITK ? (BT == 256 ? 3 : 2) : 1;
     return BT == 256 ? 3 : 6;
 }
 
 template <int BT, int KIND, bool SPLITK, bool F32OUT>
-using SwapKernel = Launcher<fg::fp8_gemm_swap_kernel<BT, swap_stages<BT>(), KIND, SPLITK, F32OUT>,
-                            fg::SwapSmemLayout<BT, swap_stages<BT>()>::BYTES, SPLITK>;
+using SwapKernel = Launcher<fg::fp8_gemm_swap_kernel<BT, swap_stages<BT, SPLITK>(), KIND, SPLITK, F32OUT>,
+                            fg::SwapSmemLayout<BT, swap_stages<BT, SPLITK>()>::BYTES, SPLITK>;
 
 // Estimated time (us) of a swapped plan, in the form of the one-CTA plan model
 // (start-up + the larger of HBM time and per-SM operand intake + split-K

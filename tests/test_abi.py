@@ -33,6 +33,26 @@ def test_library_exports_every_declared_symbol():
     assert set(declared_functions()) <= set(fg.SIGNATURES)
 
 
+def test_debug_build_exports_the_same_symbols_and_says_so():
+    """libfp8gemm_debug.so (FG_DEBUG: device-side bounds checks, single-stage
+    pipelines) is a drop-in for the library: same C ABI; it reports itself
+    as the debug build and accepts the coordinate hook the release build
+    refuses."""
+    h = fg.lib(debug=True)
+    assert os.path.basename(fg.library_path(True)) == "libfp8gemm_debug.so"
+    for name in declared_functions():
+        assert hasattr(h, name), name
+    assert h.fg_debug_build() == 1 and fg.lib(debug=False).fg_debug_build() == 0
+    assert fg.lib(debug=False).fg_debug_bad_coordinate(0) == 3  # FG_ERR_UNSUPPORTED
+    assert h.fg_debug_bad_coordinate(-1) == 0
+    fg.use_debug_library(True)
+    try:
+        assert fg.lib() is h and fg.fg_version() >= 100
+    finally:
+        fg.use_debug_library(False)
+    assert fg.lib() is not h
+
+
 def test_host_only_helpers():
     assert fg.fg_scales_a_ld(1) == 4 and fg.fg_scales_a_ld(4) == 4 and fg.fg_scales_a_ld(130) == 132
     assert fg.fg_status_string(0) == "FG_OK" and fg.fg_status_string(5) == "FG_ERR_TIMEOUT"
