@@ -220,6 +220,31 @@ def test_masked_counts_read_on_device_only():
     assert st == 0
 
 
+@pytest.mark.parametrize("plan", ["auto", "one_cta_128", "split3_256", "pair"])
+def test_masked_many_groups(plan):
+    """128 groups (the expert counts of large MoE layers): every tile walks the
+    device-side counts of all groups to find its own; counts 0 and M_cap among
+    them, rows past each count untouched, the rest against the oracle."""
+    bn, split, pair = {"auto": (0, 0, -1), "one_cta_128": (128, 1, 0), "split3_256": (256, 3, 0),
+                       "pair": (256, 1, 1)}[plan]
+    G, M_cap = 128, 192
+    counts = wl.rng_for(71).integers(0, M_cap, size=G, endpoint=True)
+    counts[:4] = [0, M_cap, 1, 128]
+    p = wl.masked(G, M_cap, n=264, k=384, seed=72, masked_m=counts)
+    fg.fg_set_config_override(bn, split)
+    fg.fg_set_pair_mode(pair)
+    try:
+        got = d_to_bits(run_masked(p))
+    finally:
+        fg.fg_set_config_override(0, 0)
+        fg.fg_set_pair_mode(-1)
+    init = np.full((p.G, p.M_cap, p.n), SENTINEL, np.uint16)
+    ref, _ = oracle.grouped_masked(p.A, 0, p.sA, p.B, 0, p.sB, p.masked_m, init)
+    valid = np.arange(M_cap)[None, :] < p.masked_m[:, None]
+    assert np.array_equal(got[~valid], ref[~valid]), "rows past the count were written"
+    compare(got[valid], ref[valid], what=f"masked G=128 ({plan})")
+
+
 @pytest.mark.parametrize("G,n,k", wl.masked_shapes())
 def test_masked_workload(G, n, k):
     """G groups of capacity 256 with seeded uniform counts; rows past the counts
