@@ -181,9 +181,12 @@ bool fmt_ok(int f) { return f == FG_E4M3 || f == FG_E5M2; }
 
 // M blocks per raster group: as many as keep the group's A rows (128 x k bytes
 // per block) within about 48 MiB of L2, so B is streamed once per group while
-// A stays resident.  Masked problems walk few M blocks: one group.
+// A stays resident.  Masked problems walk N fastest (raster groups of one M
+// block): a CTA's tiles then visit the valid M blocks in increasing order, so
+// each role finds a tile's group with a forward scan over the counts, and a
+// group's weights, read once per M block, are still in L2 for its next one.
 int raster_group_m(int kind, int m_blocks, int k) {
-    if (kind == fg::KIND_MASKED) return m_blocks > 0 ? m_blocks : 1;
+    if (kind == fg::KIND_MASKED) return 1;
     const long long per_block = (long long)fg::BLOCK_M * k;
     long long g = (48ll << 20) / (per_block > 0 ? per_block : 1);
     if (g < 1) g = 1;

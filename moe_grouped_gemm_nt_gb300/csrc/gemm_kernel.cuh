@@ -196,12 +196,15 @@ struct Tile {
     int kb_lo, kb_hi;  // K-grouped layout: the tile's K blocks (its group's segment)
 };
 
-// K-grouped layout: position of the scan over the segment lengths (group g
-// starts at K block kb).  Every role walks its tiles in increasing order, and
-// the tiles of one group are consecutive, so the scan only moves forward.
-struct KScan {
+// Position of a role's scan over the groups' device-side sizes: group g
+// begins at block `first` (K-grouped layout: its first K block; masked
+// layout: its first valid M block, or 256-row block on CTA pairs).  Every
+// role visits its tiles in increasing order and the tiles of one group are
+// consecutive, so the scan moves forward: O(G + tiles) loads per CTA, where a
+// scan from group 0 for every tile would cost O(G) per tile.
+struct GroupScan {
     int g = 0;
-    int kb = 0;
+    int first = 0;
 };
 
 __device__ __forceinline__ int k_segment_blocks(const GemmParams &p, int g) {
@@ -230,7 +233,7 @@ __device__ __forceinline__ int total_m_blocks(const GemmParams &p) {
 // K-grouped layout: the tiles of group g (all M x N blocks of its output) come
 // before those of group g + 1, each group walked like a dense problem.
 template <int BN, int KIND>
-__device__ __forceinline__ Tile get_tile(const GemmParams &p, int t, int mblocks, KScan &scan) {
+__device__ __forceinline__ Tile get_tile(const GemmParams &p, int t, int mblocks, GroupScan &scan) {
     Tile ti;
     ti.kb_lo = 0;
     ti.kb_hi = p.num_kb;
@@ -238,10 +241,10 @@ __device__ __forceinline__ Tile get_tile(const GemmParams &p, int t, int mblocks
         const int per_g = mblocks * p.num_n_blocks;
         const int g = t / per_g;
         t -= g * per_g;
-        if (g < scan.g) scan = KScan{};
-        while (scan.g < g) scan.kb += k_segment_blocks(p, scan.g++);
-        ti.kb_lo = min(scan.kb, p.num_kb);
-        ti.kb_hi = min(scan.kb + k_segment_blocks(p, g), p.num_kb);
+        if (g < scan.g) scan = GroupScan{};
+        while (scan.g < g) scan.first += k_segment_blocks(p, scan.g++);
+        ti.kb_lo = min(scan.first, p.num_kb);
+        ti.kb_hi = min(scan.first + k_segment_blocks(p, g), p.num_kb);
         ti.group = g;
     }
     const int per_group = p.group_m * p.num_n_blocks;
@@ -269,13 +272,17 @@ __device__ __forceinline__ Tile get_tile(const GemmParams &p, int t, int mblocks
         ti.b_row = g * p.n + ti.n_blk * BN;
         ti.row_limit = BLOCK_M;
     } else {
-        int g = 0, acc = 0, cnt = 0;
+        // the group holding valid M block mb_lin, by the role's forward scan
+        if (mb_lin < scan.first) scan = GroupScan{};
+        int g = scan.g, acc = scan.first, cnt = 0;
         for (; g < p.num_groups; ++g) {
             cnt = clamp_count(__ldg(p.masked_m + g), p.rows);
             const int nb = (cnt + BLOCK_M - 1) / BLOCK_M;
             if (mb_lin < acc + nb) break;
             acc += nb;
         }
+        scan.g = g;
+        scan.first = acc;
         ti.valid = g < p.num_groups;
         ti.group = g;
         ti.m_blk = mb_lin - acc;
@@ -487,7 +494,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (lane == 0) {
             uint32_t it = 0;
             bool ok = true;
-            KScan scan;
+            GroupScan scan;
             for (int t = t_begin; t < num_tiles && ok; t += t_step) {
                 const Tile ti = get_tile<BN, KIND>(p, t, m_blocks, scan);
                 if (!ti.valid) continue;
@@ -557,7 +564,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (lane == 0) {
             uint32_t it = 0;
             bool ok = true;
-            KScan scan;
+            GroupScan scan;
             for (int t = t_begin; t < num_tiles && ok; t += t_step) {
                 const Tile ti = get_tile<BN, KIND>(p, t, m_blocks, scan);
                 if (!ti.valid) continue;
@@ -612,7 +619,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // scale-ring entry q (phase qph) of the current K iteration
         uint32_t b = 0, bph = 0, q = 0, qph = 0;
         bool ok = true;
-        KScan scan;
+        GroupScan scan;
         for (int t = t_begin; t < num_tiles && ok; t += t_step) {
             const Tile ti = get_tile<BN, KIND>(p, t, m_blocks, scan);
             if (!ti.valid) {
@@ -828,7 +835,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 any_abort |= ld_shared_cluster_u32(map_shared_rank(smem_u32((const void *)abort_flag), q)) != 0u;
             const bool tile_ok = t_begin < num_tiles && !any_abort;
             if (tile_ok && warp < NUM_EPI_WARPS) {
-                KScan scan;
+                GroupScan scan;
                 const Tile ti = get_tile<BN, KIND>(p, t_begin, m_blocks, scan);
                 if (ti.valid) {
                     constexpr int CH = BN / 4;  // 16-byte chunks per partial row

@@ -88,7 +88,7 @@ __device__ __forceinline__ int total_pair_blocks(const GemmParams &p) {
 // before those of group g + 1, the K range from the forward scan of get_tile().
 template <int KIND>
 __device__ __forceinline__ PairTile get_pair_tile(const GemmParams &p, int t, int pblocks, uint32_t rank,
-                                                  KScan &scan) {
+                                                  GroupScan &scan) {
     PairTile ti;
     ti.kb_lo = 0;
     ti.kb_hi = p.num_kb;
@@ -97,10 +97,10 @@ __device__ __forceinline__ PairTile get_pair_tile(const GemmParams &p, int t, in
         const int per_g = pblocks * p.num_n_blocks;
         const int g = t / per_g;
         t -= g * per_g;
-        if (g < scan.g) scan = KScan{};
-        while (scan.g < g) scan.kb += k_segment_blocks(p, scan.g++);
-        ti.kb_lo = min(scan.kb, p.num_kb);
-        ti.kb_hi = min(scan.kb + k_segment_blocks(p, g), p.num_kb);
+        if (g < scan.g) scan = GroupScan{};
+        while (scan.g < g) scan.first += k_segment_blocks(p, scan.g++);
+        ti.kb_lo = min(scan.first, p.num_kb);
+        ti.kb_hi = min(scan.first + k_segment_blocks(p, g), p.num_kb);
         ti.group = g;
     }
     const int per_group = p.group_m * p.num_n_blocks;
@@ -112,13 +112,17 @@ __device__ __forceinline__ PairTile get_pair_tile(const GemmParams &p, int t, in
     ti.n_blk = rem / gm;
     const int half = (int)rank * BLOCK_M;
     if constexpr (KIND == KIND_MASKED) {
-        int g = 0, acc = 0, cnt = 0;
+        // the group holding valid 256-row block pb_lin, by the role's forward scan
+        if (pb_lin < scan.first) scan = GroupScan{};
+        int g = scan.g, acc = scan.first, cnt = 0;
         for (; g < p.num_groups; ++g) {
             cnt = clamp_count(__ldg(p.masked_m + g), p.rows);
             const int nb = (cnt + PAIR_ROWS - 1) / PAIR_ROWS;
             if (pb_lin < acc + nb) break;
             acc += nb;
         }
+        scan.g = g;
+        scan.first = acc;
         ti.valid = g < p.num_groups;
         ti.group = g;
         const int row0 = (pb_lin - acc) * PAIR_ROWS + half;  // within the group
@@ -260,7 +264,7 @@ __global__ void __launch_bounds__(DEFER ? PAIR_DEFER_THREADS : NUM_THREADS, 1)
         if (lane == 0) {
             uint32_t it = 0;
             bool ok = true;
-            KScan scan;
+            GroupScan scan;
             for (int t = t_begin; t < num_tiles && ok; t += t_step) {
                 const PairTile ti = get_pair_tile<KIND>(p, t, pblocks, rank, scan);
                 if (!ti.valid) continue;
@@ -333,7 +337,7 @@ __global__ void __launch_bounds__(DEFER ? PAIR_DEFER_THREADS : NUM_THREADS, 1)
         if (leader && lane == 0) {
             uint32_t it = 0;
             bool ok = true;
-            KScan scan;
+            GroupScan scan;
             for (int t = t_begin; t < num_tiles && ok; t += t_step) {
                 const PairTile ti = get_pair_tile<KIND>(p, t, pblocks, rank, scan);
                 if (!ti.valid) continue;
@@ -385,7 +389,7 @@ __global__ void __launch_bounds__(DEFER ? PAIR_DEFER_THREADS : NUM_THREADS, 1)
         uint32_t b = 0, bph = 0, q = 0, qph = 0;
         uint32_t ep = 0;  // DEFER: tiles staged so far (parity of the staging barriers)
         bool ok = true;
-        KScan scan;
+        GroupScan scan;
         for (int t = t_begin; t < num_tiles && ok; t += t_step) {
             const PairTile ti = get_pair_tile<KIND>(p, t, pblocks, rank, scan);
             if (!ti.valid) continue;
@@ -576,7 +580,7 @@ __global__ void __launch_bounds__(DEFER ? PAIR_DEFER_THREADS : NUM_THREADS, 1)
         // it back.
         if (lane == 0) {
             uint32_t ep = 0;
-            KScan scan;
+            GroupScan scan;
             for (int t = t_begin; t < num_tiles; t += t_step) {
                 const PairTile ti = get_pair_tile<KIND>(p, t, pblocks, rank, scan);
                 if (!ti.valid) continue;
