@@ -391,9 +391,9 @@ def measure_other_configs(fg, torch, dev, stream, fp8_peak, hbm_peak, peak_src, 
         out["large_dense"].append(row(f"{m}x{n}x{k} B={'E5M2' if bfmt else 'E4M3'}", us, 2.0 * m * n * k, byts))
         del copies
     # K-grouped (the weight gradient of the contiguous workload): G segments of
-    # 8192 tokens, D [G][M][N] in BF16
+    # 8192 tokens, and 32 short segments of 512 tokens; D [G][M][N] in BF16
     out["k_grouped"] = []
-    for (G, M, N, tok) in wl.k_grouped_shapes():
+    for (G, M, N, tok) in wl.k_grouped_shapes() + wl.k_grouped_short_shapes():
         K = G * tok
         kb, nb = (K + 127) // 128, (N + 127) // 128
         byts = M * K + N * K + G * M * N * 2

@@ -152,13 +152,16 @@ def test_k_grouped_bad_segment_lengths_are_reported(ks, detail, plan):
     check_status()
 
 
-@pytest.mark.parametrize("G,M,N,tokens", wl.k_grouped_shapes()[:2])
+@pytest.mark.parametrize("G,M,N,tokens", wl.k_grouped_shapes()[:2] + wl.k_grouped_short_shapes())
 def test_k_grouped_workload(G, M, N, tokens):
-    """The weight gradient of the contiguous workload: G experts of 8192 tokens,
-    M = n, N = k of the forward weight, checked on sampled outputs of every
-    group's plane (the first and last planes' corner and boundary tiles in full)."""
+    """The weight gradient of the contiguous workload (G experts of 8192 tokens;
+    or 32 experts of 512, the short-segment plan on CTA pairs with the store
+    warp), M = n, N = k of the forward weight, checked on sampled outputs of
+    every group's plane (the first and last planes' corner and boundary tiles
+    in full)."""
     ks = [tokens] * G
-    p = wl.k_grouped(M, N, ks, seed=wl.seed_for(6, wl.k_grouped_shapes().index((G, M, N, tokens))))
+    shapes = wl.k_grouped_shapes() + wl.k_grouped_short_shapes()
+    p = wl.k_grouped(M, N, ks, seed=wl.seed_for(6, shapes.index((G, M, N, tokens))))
     D = d_to_bits(_run(p, ks))
     full = sample_positions(M, N, seed=G + M, n_rows_full=2, boundary_tiles=True)
     light = sample_positions(M, N, seed=G + M + 1, n_rows_full=2)
@@ -198,3 +201,27 @@ def test_k_grouped_pair_tiles_workload_sampled():
     ref16, _ = oracle.k_grouped_at(p.A, 0, p.sA, p.B, 0, p.sB, np.array(ks, np.int32), gs, rr, cc)
     compare(D[gs, rr, cc], ref16, what="k-grouped pair tiles (sampled)")
     assert not np.any(D[1]), "empty segment must give zeros"
+
+
+@pytest.mark.parametrize("plan", ["auto", "one_cta_256", "cta_pair_deferred"])
+def test_k_grouped_many_short_segments(plan):
+    """128 groups of one or two K blocks each (and some empty ones): every
+    role's forward scan over the segment lengths walks all 128 groups, full
+    comparison with the oracle."""
+    name = plan
+    if name != "auto":
+        fg.fg_set_config_override(256, 1)
+        fg.fg_set_pair_mode(0 if name == "one_cta_256" else 1)
+        fg.lib().fg_debug_set_pair_defer(1 if name == "cta_pair_deferred" else 0)
+    try:
+        rng = wl.rng_for(77)
+        ks = (rng.integers(0, 3, size=128) * 128).tolist()
+        ks[:3] = [0, 256, 128]
+        p = wl.k_grouped(288, 264, ks, seed=78)
+        D = _run(p, ks)
+    finally:
+        fg.fg_set_config_override(0, 0)
+        fg.fg_set_pair_mode(-1)
+        fg.lib().fg_debug_set_pair_defer(-1)
+    ref16, _ = oracle.k_grouped(p.A, 0, p.sA, p.B, 0, p.sB, np.array(ks, np.int32))
+    compare(d_to_bits(D), ref16, what=f"k-grouped 128 short segments ({plan})")

@@ -366,6 +366,16 @@ def k_grouped_shapes():
     return [(G, n, k, KGROUPED_TOKENS_PER_GROUP) for G in KGROUPED_G for (n, k) in GROUPED_NK]
 
 
+# short segments: many experts with few tokens each (the CTA-pair plan with the store warp)
+KGROUPED_SHORT_G = 32
+KGROUPED_SHORT_TOKENS = 512
+
+
+def k_grouped_short_shapes():
+    """(G, M, N, tokens per group) of the short-segment K-grouped figures."""
+    return [(KGROUPED_SHORT_G, n, k, KGROUPED_SHORT_TOKENS) for (n, k) in GROUPED_NK]
+
+
 def k_grouped(M, N, k_sizes, seed, b_fmt=E4M3, K=None) -> Dense:
     """Operands of a K-grouped problem: A [M][K], B [N][K] with the NT GEMM's
     scaling (1 x 128 LHS groups, 128 x 128 RHS blocks), K = sum of the segment
