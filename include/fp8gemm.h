@@ -40,8 +40,15 @@
  *   k % 128 columns; the scale of that block still applies.
  * - Errors found on the host are returned at once (nothing is launched).
  *   Errors found by the kernel (a wait that exceeded the watchdog limit, a
- *   group id or count out of range) are recorded in a per-device status word
- *   and read with fg_get_device_status().
+ *   group id, count or segment length out of range) are recorded in a
+ *   per-device status word and read with fg_get_device_status().
+ * - The same ABI is exported by the FG_DEBUG build of the library
+ *   (libfp8gemm_debug.so): single-stage pipelines and a device-side check of
+ *   every TMA box start, ring index and TMEM column before use.  A failed
+ *   check records FG_ERR_DEVICE_CHECK with a tag in bits 24..31 of the detail
+ *   (0x41 A or LHS-scale box, 0x42 B box, 0x43 D box, 0x44 ring slot, 0x45
+ *   TMEM columns, 0x46 a non-finite K-block partial) and the offending value
+ *   in bits 0..23, and the access is skipped.  For bisecting races, not speed.
  */
 #ifndef FP8GEMM_H_
 #define FP8GEMM_H_
