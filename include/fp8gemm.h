@@ -151,11 +151,10 @@ fg_status fg_grouped_gemm_fp8_masked_f32out(const void *A, int a_fmt, const floa
  *   D   [G][M][N] bfloat16 (the _f32out form: float), 16-byte aligned; every
  *       element is written (an empty segment gives zeros).
  * K % 16 == 0, N % 8 == 0; M == 0 is a no-op.  Tiles: for the BF16 form
- * with M >= 256 and segments of at most 16 K blocks on average, 256 x 256 on
- * CTA pairs (with the store warp from 4 K blocks on average; measured faster
- * there, while one-CTA tiles are faster on longer segments), else 128 x 256
- * or, when those would leave SMs idle, 128 x 128 on one CTA; fg_query_plan
- * with kind 3 reports the choice. */
+ * with M >= 256, 256 x 256 on CTA pairs (with the store warp when the
+ * segments average 4 to 12 K blocks, where it measured faster), else
+ * 128 x 256 or, when those would leave SMs idle, 128 x 128 on one CTA;
+ * fg_query_plan with kind 3 reports the choice. */
 fg_status fg_k_grouped_gemm_fp8_nt(const void *A, int a_fmt, const float *sA, int ld_sA,
                                    const void *B, int b_fmt, const float *sB, void *D,
                                    const int32_t *k_sizes, int G, int M, int N, int K, void *stream);
@@ -275,7 +274,7 @@ fg_status fg_set_swap_mode(int mode);
  * per tile), [1] the split-K cluster size (1 = none), [2] 1 for CTA-pair
  * tiles, [3] 1 for swapped operand roles, [4] 1 when the CTA-pair tiles of a
  * BF16 call stage a whole tile and a store warp issues its stores (tiles of
- * at most 16 K blocks, K-grouped: 4 to 16 on average; the FP32 output forms
+ * at most 56 K blocks, K-grouped: 4 to 12 on average; the FP32 output forms
  * never do).  Host-only (reads device attributes, launches nothing). */
 fg_status fg_query_plan(int kind, int rows, int G, int n, int k, int *plan);
 

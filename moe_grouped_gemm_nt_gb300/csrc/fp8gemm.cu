@@ -95,12 +95,20 @@ template <int KIND>
 using PairDeferKernel = Launcher<fg::fp8_gemm_pair_kernel<KIND, kPairDeferStages, kPairScaleStages, false, true>,
                                  fg::PairSmemLayout<kPairDeferStages, kPairScaleStages, true>::BYTES, true,
                                  fg::PAIR_DEFER_THREADS>;
-// -1: deferred stores for tiles of at most kPairDeferMaxKb K blocks (measured:
-// 4096 x 24576 x 1536 137.8 -> 128.9 us, 4096 x 7168 x 2048 56.0 -> 54.1 us;
-// with 56 or more K blocks the fifth operand stage is worth more: 4096 x 7168
-// x 16384 333.8 -> 340.5 us); 0 never; 1 always
+// -1: deferred stores for dense (and masked) tiles of at most kPairDeferMaxKb
+// K blocks and for K-grouped segments of kKgDeferMinKb to kKgDeferMaxKb K
+// blocks on average; 0 never; 1 always.  Measured on CTA pairs (graph-timed,
+// without -> with the store warp, which costs the fifth operand stage): dense
+// 4096 x 24576 x 1536 135.5 -> 120.7 us, 4096 x 7168 x 2048 51.9 -> 49.1,
+// 4096 x 7168 x 4096 89.6 -> 87.1, 4096 x 4096 x 7168 99.4 -> 98.1, 4096 x 7168
+// x 7168 146.7 -> 144.6; 8192^3 385.6 -> 386.8, 4096 x 7168 x 16384 324.6 ->
+// 329.1.  K-grouped, 8 groups of 4096 x 7168: 1024 tokens each 244.8 -> 228.6,
+// 1536: 323.5 -> 322.1, 1792: 362.9 -> 365.1, 2048: 401.4 -> 411.8; segments of
+// 2 K blocks: 32 groups of 4096 x 7168 with 256 tokens 371.3 -> 394.5.
 std::atomic<int> g_pair_defer{-1};
-constexpr int kPairDeferMaxKb = 16;
+constexpr int kPairDeferMaxKb = 56;
+constexpr int kKgDeferMinKb = 4;
+constexpr int kKgDeferMaxKb = 12;
 
 // Tile plan of one call: output tile width and split-K factor.
 struct Plan {
@@ -333,9 +341,9 @@ fg_status run(const void *A, int a_fmt, const float *sA, int ld_sA, const void *
 // K-grouped entry points: G groups, each an NT product over its own segment of
 // K (segment lengths on the device), all sharing A [M][K] and B [N][K]; output
 // planes D [G][M][N].  Persistent tiles, no split-K: 256 x 256 on CTA pairs
-// with the store warp for short segments (BF16 output, M >= 256, the 256-wide
-// tiles filling the SMs), else one-CTA 128 x 256 (or 128 x 128 when the
-// 256-wide tiles would leave SMs idle).
+// (BF16 output, M >= 256, the 256-wide tiles filling the SMs; the store warp
+// for segments of 4 to 12 K blocks on average), else one-CTA 128 x 256 (or
+// 128 x 128 when the 256-wide tiles would leave SMs idle).
 struct KgPlan {
     int bn = 256;
     bool pair = false;
@@ -348,21 +356,21 @@ KgPlan kgrouped_plan(int G, int M, int N, int K, int sms, bool f32out) {
     const long long tiles256 = (long long)G * cdiv(M, fg::BLOCK_M) * cdiv(N, 256);
     const int fbn = g_force_bn.load();
     if (fbn == 128 || (fbn == 0 && tiles256 * 4 < (long long)sms * 3)) kp.bn = 128;
-    // CTA pairs when the segments are short (at most kPairDeferMaxKb K blocks
-    // on average), with the store warp unless they are shorter than 4 K
-    // blocks; one-CTA tiles otherwise.  Measured (BF16 output; one CTA / pairs
-    // / pairs with the store warp): 8 groups of 4096 x 7168 with 1024 tokens
-    // each 253.8 / 264.8 / 238.7 us; 16 of 2048 x 2048 with 512 tokens 52.6 /
-    // 53.9 / 46.8 us; 32 of 4096 x 7168 with 256 tokens 395.8 / 385.6 / 405.2
-    // us; with 8192 tokens per group one-CTA tiles win (8 of 4096 x 7168: 1449
-    // against 1605 / 1633 us).
+    // CTA pairs for BF16 output with M >= 256, whatever the segment lengths,
+    // with the store warp when the segments average kKgDeferMinKb to
+    // kKgDeferMaxKb K blocks.  Measured (graph-timed; one CTA / pairs / pairs
+    // with the store warp): 4 groups of 4096 x 7168 with 8192 tokens each
+    // 728.5 / 690.4 / 792.5 us; 8 of 7168 x 2048 with 8192 tokens 753.6 /
+    // 711.9 / 822.9; 8 of 4096 x 7168 with 2048 tokens 417.6 / 404.9 / 414.5,
+    // with 1024 tokens 253.4 / 248.3 / 230.8; 32 of 4096 x 7168 with 512 tokens
+    // 629.2 / 637.3 / 519.7, with 256 tokens 395.0 / 371.3 / 394.5.
     const long long kb_total = cdiv(K, fg::BLOCK_K);
-    const bool short_segments = kb_total <= (long long)kPairDeferMaxKb * G;
     const int pmode = g_pair_mode.load();
     kp.pair = sms >= 2 && kp.bn == 256 && pmode != 0 &&
-              (pmode == 1 || (fbn == 0 && M >= fg::PAIR_ROWS && !f32out && short_segments));
+              (pmode == 1 || (fbn == 0 && M >= fg::PAIR_ROWS && !f32out));
     const int dmode = g_pair_defer.load();
-    kp.defer = kp.pair && !f32out && (dmode == 1 || (dmode < 0 && short_segments && kb_total >= 4ll * G));
+    const bool defer_len = kb_total >= (long long)kKgDeferMinKb * G && kb_total <= (long long)kKgDeferMaxKb * G;
+    kp.defer = kp.pair && !f32out && (dmode == 1 || (dmode < 0 && defer_len));
     return kp;
 }
 

@@ -249,8 +249,10 @@ def test_pair_plan_query():
 
     assert fg.fg_query_dense_plan_ex(4096, 7168, 2048)[2] == 1
     assert fg.fg_query_dense_plan_ex(128, 7168, 2048)[2] == 0
-    # BF16 pair tiles of at most 16 K blocks store through the eleventh warp
+    # BF16 pair tiles of at most 56 K blocks store through the eleventh warp
     assert fg.fg_query_plan(0, 4096, 1, 7168, 2048)[2:] == (1, 0, 1)
+    assert fg.fg_query_plan(0, 4096, 1, 4096, 7168)[2:] == (1, 0, 1)
+    assert fg.fg_query_plan(0, 4096, 1, 7168, 7296)[2:] == (1, 0, 0)
     assert fg.fg_query_plan(0, 4096, 1, 7168, 16384)[2:] == (1, 0, 0)
 
 

@@ -174,7 +174,9 @@ def test_k_grouped_workload(G, M, N, tokens):
 
 
 @pytest.mark.parametrize("G,M,N,K,want", [
-    (4, 4096, 7168, 4 * 8192, (256, 1, 0, 0, 0)),    # segments of 64 K blocks: one-CTA tiles
+    (4, 4096, 7168, 4 * 8192, (256, 1, 1, 0, 0)),    # segments of 64 K blocks: CTA pairs, promotion warps store
+    (8, 4096, 7168, 8 * 2048, (256, 1, 1, 0, 0)),    # segments of 16: the same
+    (8, 4096, 7168, 8 * 1536, (256, 1, 1, 0, 1)),    # segments of 12: CTA pairs with the store warp
     (8, 4096, 2048, 8 * 1024, (256, 1, 1, 0, 1)),    # segments of 8: CTA pairs with the store warp
     (2, 128, 512, 2 * 1024, (128, 1, 0, 0, 0)),      # a few one-CTA tiles: 128 wide
     (8, 200, 4096, 8 * 512, (256, 1, 0, 0, 0)),      # fewer than 256 rows: one-CTA tiles
