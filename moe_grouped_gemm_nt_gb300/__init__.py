@@ -404,7 +404,8 @@ def fg_set_pair_mode(mode: int) -> None:
 
 
 def fg_set_swap_mode(mode: int) -> None:
-    """-1: swapped operand roles where they apply (default: masked, M_cap <= 256); 0: never; 1: wherever allowed."""
+    """Swapped operand roles (dense m <= 256, masked M_cap <= 256): -1 automatic, which never picks them
+    (measured slower on every problem); 0 never; 1 wherever they apply."""
     _check("fg_set_swap_mode", lib().fg_set_swap_mode(int(mode)))
 
 

@@ -32,7 +32,7 @@ extern std::atomic<int> g_force_bn;
 extern std::atomic<int> g_pdl;  // programmatic dependent launch of the GEMM kernels
 extern std::atomic<int> g_force_split;
 extern std::atomic<int> g_pair_mode;  // CTA-pair tiles: -1 where they apply, 0 never, 1 whenever allowed
-extern std::atomic<int> g_swap_mode;  // swapped operand roles: -1 where they apply, 0 never, 1 whenever allowed
+extern std::atomic<int> g_swap_mode;  // swapped operand roles: -1 automatic (never), 0 never, 1 wherever they apply
 extern std::atomic<int> g_debug_bad_coord;  // debug build: K iteration whose A load is sent past K (-1: none)
 
 // Per-device facts read once.  `ready` is published with release after the
