@@ -240,15 +240,16 @@ fg_status fg_query_dense_plan(int m, int n, int k, int *block_n, int *split_k);
 fg_status fg_query_dense_plan_ex(int m, int n, int k, int *block_n, int *split_k, int *cta_pair);
 
 /* CTA-pair tiles for later calls: -1 (default) where they apply (persistent
- * 256-wide dense plans with at least 256 rows, K-grouped BF16 calls with short
- * segments as described there; no forced plan), 0 never, 1 for every
- * persistent 256-wide dense, masked or K-grouped plan.  The contiguous layout
- * always uses 128-row tiles (two adjacent 128-row blocks may belong to two
- * groups; measured, pairing them with a second pass for such blocks was
- * slower than 128-row tiles).  The masked layout uses 128-row tiles unless
- * the mode is 1 (a 256-row tile also computes a group's empty rows past its
- * count; measured slower).  Results differ between the modes only by FP32
- * summation order; FG_ERR_INVALID_ARG for other values. */
+ * 256-wide dense plans with at least 256 rows, K-grouped BF16 calls with at
+ * least 256 rows; no forced plan), 0 never, 1 for every persistent 256-wide
+ * plan of any layout.  The contiguous and masked layouts use 128-row tiles
+ * unless the mode is 1.  Contiguous: a pair tile whose two 128-row blocks
+ * belong to two groups runs once per group, each pass storing its group's
+ * rows; measured within about 2% of 128-row tiles on the contiguous workloads
+ * and 21% slower when every pair straddles two groups.  Masked: a 256-row tile
+ * also computes a group's empty rows past its count; measured slower.  Results
+ * differ between the modes only by FP32 summation order (measured bitwise
+ * equal on the contiguous workloads); FG_ERR_INVALID_ARG for other values. */
 fg_status fg_set_pair_mode(int mode);
 
 /* Swapped operand roles ("swap-AB") for later calls: the weights (B) take the

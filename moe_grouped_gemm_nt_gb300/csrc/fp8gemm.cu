@@ -204,20 +204,24 @@ int raster_group_m(int kind, int m_blocks, int k) {
 
 // Whether a call runs on CTA pairs (256 x 256 tiles): by default, persistent
 // 256-wide dense plans with at least 256 rows, unless a tile plan is forced;
-// with the pair mode at 1, every persistent 256-wide dense or masked plan.
-// The contiguous layout keeps 128-row tiles: two adjacent 128-row blocks may
-// belong to different groups, which one pair MMA (one B) cannot serve.  The
-// masked layout keeps them by default: a group's valid rows rarely fill 256,
+// with the pair mode at 1, every persistent 256-wide plan.  The contiguous
+// layout keeps 128-row tiles by default: on pairs (a tile whose two 128-row
+// blocks belong to different groups runs once per group) it measured within
+// 2% of them either way (graph-timed, one CTA / pairs / pairs with the store
+// warp: 4 groups of 8192 rows x 4096 x 7168 715.2 / 698.8 / 700.3 us, 8 groups
+// 1433.5 / 1454.8 / 1494.9, 8 x 8192 rows x 7168 x 2048 807.7 / 821.2 / 805.0)
+// and 21% slower when every pair holds two groups (64 groups of 128 rows x
+// 7168 x 2048: 176.4 / 212.9 / 218.0).  The masked layout keeps them by default: a group's valid rows rarely fill 256,
 // and a 256-row tile computes and loads its empty lower half where a 128-row
 // block past the count is skipped (measured on the masked workloads with
 // capacity 256: 16 groups take 108 us on 128-row tiles against 133 us on
 // pairs for n = 4096, 63 against 72 us for n = 7168).
 bool use_pair(int kind, const Plan &plan, int rows) {
-    if (kind == fg::KIND_CONTIGUOUS || plan.split != 1 || plan.bn != 256) return false;
+    if (plan.split != 1 || plan.bn != 256) return false;
     const int mode = g_pair_mode.load();
     if (mode == 0) return false;
     if (mode == 1) return true;
-    if (kind == fg::KIND_MASKED) return false;
+    if (kind == fg::KIND_MASKED || kind == fg::KIND_CONTIGUOUS) return false;
     if (g_force_bn.load() != 0 || g_force_split.load() != 0) return false;
     return rows >= fg::PAIR_ROWS;
 }
@@ -296,7 +300,7 @@ fg_status run(const void *A, int a_fmt, const float *sA, int ld_sA, const void *
     p.b_rows_total = G * n;
     p.debug_bad_coord = g_debug_bad_coord.exchange(-1);
 
-    if constexpr (KIND != fg::KIND_CONTIGUOUS) {
+    {
         if (pair) {
             // 256 x 256 tiles on CTA pairs: the raster counts 256-row blocks
             // (whose A rows take twice the bytes of a 128-row block)

@@ -19,8 +19,14 @@
 //     like the one-CTA kernel; they hand the TMEM buffer back by arriving on
 //     the even CTA's `tmem_empty[b]` (16 arrivals: 8 warps per CTA).
 //
-// Dense and masked layouts (the masked walk pairs 128-row blocks inside a
-// group; rows past a group's count are loaded but never stored).  Every wait
+// Dense, masked, K-grouped and contiguous layouts (the masked walk pairs
+// 128-row blocks inside a group; rows past a group's count are loaded but
+// never stored).  Contiguous layout: a pair tile covers 128-row blocks 2p and
+// 2p + 1, which may belong to different groups (segments are 128-aligned) and
+// one MMA multiplies both by one group's weights, so a tile takes one pass per
+// group present: the group of block 2p, then that of block 2p + 1 if it is
+// another; a pass stores only the rows of its group (the group id of each row
+// decides, which also leaves the -1 padding rows untouched).  Every wait
 // is bounded by the same watchdog as the one-CTA kernel; both CTAs always
 // reach the final cluster barrier, so neither leaves while the other (or the
 // even CTA's MMAs) may still use its shared memory or TMEM.
@@ -54,7 +60,9 @@ struct PairSmemLayout {
     // (DEFER: + staging_full, staging_empty)
     static constexpr int NUM_BARS = 2 * STAGES + 2 * SS + 2 * NUM_TBUF + 1 + (DEFER ? 2 : 0);
     static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
-    static constexpr int BYTES = MISC_OFF + 16;
+    // TMEM address, abort flag, DEFER: one byte per promotion warp (1 = its rows
+    // of the tile are staged for the store warp, 0 = stored row by row)
+    static constexpr int BYTES = MISC_OFF + 8 + NUM_EPI_WARPS;
     static constexpr int TMEM_COLS = 512;
 };
 
@@ -67,7 +75,14 @@ struct PairTile {
     int b_row;      // first row of this CTA's half of B in the 2-D row space [G*n][k]
     int row_limit;  // rows of this CTA's half below the bound (<= 0: none)
     int kb_lo, kb_hi;  // K-grouped layout: the tile's K blocks (its group's segment)
+    int own_group;     // contiguous layout: group id of the first row of this CTA's block (-2: past M)
+    int own_pass;      // contiguous layout: this pass is the one of this CTA's block
 };
+
+// Passes per pair tile: the contiguous layout may need one per group of its
+// two 128-row blocks; the walk runs over v = tile * PASSES + pass.
+template <int KIND>
+__host__ __device__ constexpr int pair_passes() { return KIND == KIND_CONTIGUOUS ? 2 : 1; }
 
 // 256-row blocks of the whole walk (masked: of all groups' counts).
 template <int KIND>
@@ -82,17 +97,25 @@ __device__ __forceinline__ int total_pair_blocks(const GemmParams &p) {
     }
 }
 
-// Pair tile t (cluster c takes tiles c, c + clusters, ...), the half of CTA
-// `rank`; the raster is that of get_tile() over 256-row blocks.  K-grouped
-// layout: the tiles of group g (every 256-row block of its output plane)
-// before those of group g + 1, the K range from the forward scan of get_tile().
+// Pass v of the walk: pair tile t = v / pair_passes<KIND>() (cluster c takes
+// tiles c, c + clusters, ...), the half of CTA `rank`; the raster is that of
+// get_tile() over 256-row blocks.  K-grouped layout: the tiles of group g
+// (every 256-row block of its output plane) before those of group g + 1, the K
+// range from the forward scan of get_tile().
 template <int KIND>
-__device__ __forceinline__ PairTile get_pair_tile(const GemmParams &p, int t, int pblocks, uint32_t rank,
+__device__ __forceinline__ PairTile get_pair_tile(const GemmParams &p, int v, int pblocks, uint32_t rank,
                                                   GroupScan &scan) {
     PairTile ti;
     ti.kb_lo = 0;
     ti.kb_hi = p.num_kb;
     ti.group = 0;
+    ti.own_group = 0;
+    ti.own_pass = 1;
+    int t = v, pass = 0;
+    if constexpr (KIND == KIND_CONTIGUOUS) {
+        t = v >> 1;
+        pass = v & 1;
+    }
     if constexpr (KIND == KIND_KGROUPED) {
         const int per_g = pblocks * p.num_n_blocks;
         const int g = t / per_g;
@@ -130,6 +153,24 @@ __device__ __forceinline__ PairTile get_pair_tile(const GemmParams &p, int t, in
         ti.sa_row = row0;
         ti.b_row = g * p.n + ti.n_blk * PAIR_BN + half;
         ti.row_limit = min(BLOCK_M, cnt - row0);
+    } else if constexpr (KIND == KIND_CONTIGUOUS) {
+        // the groups of the tile's two 128-row blocks (first rows); pass 0 runs
+        // with the first block's group, pass 1 with the second's when it differs
+        const int blk0 = pb_lin * 2;
+        const int g0 = __ldg(p.m_indices + (size_t)blk0 * BLOCK_M);
+        const int g1 = (blk0 + 1) * BLOCK_M < p.rows ? __ldg(p.m_indices + (size_t)(blk0 + 1) * BLOCK_M) : -2;
+        const bool v0 = g0 >= 0 && g0 < p.num_groups;
+        const bool v1 = g1 >= 0 && g1 < p.num_groups && g1 != g0;
+        const int g = pass == 0 ? g0 : g1;
+        ti.valid = pass == 0 ? v0 : v1;
+        ti.group = g;
+        ti.own_group = rank == 0 ? g0 : g1;
+        ti.own_pass = pass == (int)rank;
+        const int row0 = pb_lin * PAIR_ROWS + half;
+        ti.a_row = row0;
+        ti.sa_row = row0;
+        ti.b_row = (ti.valid ? g : 0) * p.n + ti.n_blk * PAIR_BN + half;
+        ti.row_limit = min(BLOCK_M, p.rows - row0);
     } else {
         // dense, or K-grouped (A and B shared by the groups; the group picks
         // the K range and the output plane)
@@ -152,10 +193,9 @@ __global__ void __launch_bounds__(DEFER ? PAIR_DEFER_THREADS : NUM_THREADS, 1)
     fp8_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                          const __grid_constant__ CUtensorMap tmap_d, const __grid_constant__ CUtensorMap tmap_sa,
                          const GemmParams p) {
-    static_assert(KIND == KIND_DENSE || KIND == KIND_MASKED || KIND == KIND_KGROUPED,
-                  "pair tiles: dense, masked and K-grouped layouts");
     // rows of D past the bound are clipped by the tensor map (no per-row stores)
     constexpr bool CLIPPED = KIND == KIND_DENSE || KIND == KIND_KGROUPED;
+    constexpr int PASSES = pair_passes<KIND>();
     static_assert((SS & (SS - 1)) == 0, "scale ring size");
     static_assert(!(DEFER && F32OUT), "deferred stores: BF16 output");
     using L = PairSmemLayout<STAGES, SS, DEFER>;
@@ -188,6 +228,7 @@ __global__ void __launch_bounds__(DEFER ? PAIR_DEFER_THREADS : NUM_THREADS, 1)
     const uint32_t stg_empty_bar = drain_bar + 16u;  // DEFER: their stores have read the staging
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::MISC_OFF);
     volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(smem + L::MISC_OFF + 4);
+    volatile uint8_t *staged = smem + L::MISC_OFF + 8;  // DEFER, not CLIPPED: per promotion warp
 
     const int warp = __shfl_sync(0xffffffffu, (int)(threadIdx.x >> 5), 0);
     const int lane = threadIdx.x & 31;
@@ -265,6 +306,9 @@ __global__ void __launch_bounds__(DEFER ? PAIR_DEFER_THREADS : NUM_THREADS, 1)
     const int pblocks = total_pair_blocks<KIND>(p);
     const int num_tiles = pblocks * p.num_n_blocks * (KIND == KIND_KGROUPED ? p.num_groups : 1);
     const int t_begin = (int)(blockIdx.x >> 1), t_step = (int)(gridDim.x >> 1);
+    // the walk: passes v = t * PASSES + pass of this cluster's tiles t
+    const int v_begin = t_begin * PASSES, v_end = num_tiles * PASSES;
+    auto next_v = [&](int v) { return (v % PASSES == PASSES - 1) ? v + 1 + (t_step - 1) * PASSES : v + 1; };
 
     if (warp == PRODUCER_WARP) {
         // ------------------------------------------------------ TMA producer
@@ -272,8 +316,8 @@ __global__ void __launch_bounds__(DEFER ? PAIR_DEFER_THREADS : NUM_THREADS, 1)
             uint32_t it = 0;
             bool ok = true;
             GroupScan scan;
-            for (int t = t_begin; t < num_tiles && ok; t += t_step) {
-                const PairTile ti = get_pair_tile<KIND>(p, t, pblocks, rank, scan);
+            for (int v = v_begin; v < v_end && ok; v = next_v(v)) {
+                const PairTile ti = get_pair_tile<KIND>(p, v, pblocks, rank, scan);
                 if (!ti.valid) continue;
                 const int nb0 = min((ti.n_blk * BN) / 128, p.num_nb - 1);
                 const int nb1 = min((ti.n_blk * BN + BN / 2) / 128, p.num_nb - 1);
@@ -345,8 +389,8 @@ __global__ void __launch_bounds__(DEFER ? PAIR_DEFER_THREADS : NUM_THREADS, 1)
             uint32_t it = 0;
             bool ok = true;
             GroupScan scan;
-            for (int t = t_begin; t < num_tiles && ok; t += t_step) {
-                const PairTile ti = get_pair_tile<KIND>(p, t, pblocks, rank, scan);
+            for (int v = v_begin; v < v_end && ok; v = next_v(v)) {
+                const PairTile ti = get_pair_tile<KIND>(p, v, pblocks, rank, scan);
                 if (!ti.valid) continue;
                 for (int kb = ti.kb_lo; kb < ti.kb_hi; ++kb, ++it) {
                     const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
@@ -397,10 +441,40 @@ __global__ void __launch_bounds__(DEFER ? PAIR_DEFER_THREADS : NUM_THREADS, 1)
         uint32_t ep = 0;  // DEFER: tiles staged so far (parity of the staging barriers)
         bool ok = true;
         GroupScan scan;
-        for (int t = t_begin; t < num_tiles && ok; t += t_step) {
-            const PairTile ti = get_pair_tile<KIND>(p, t, pblocks, rank, scan);
-            if (!ti.valid) continue;
-            const bool row_ok = r < ti.row_limit;
+        for (int v = v_begin; v < v_end && ok; v = next_v(v)) {
+            const PairTile ti = get_pair_tile<KIND>(p, v, pblocks, rank, scan);
+            if (!ti.valid) {
+                if constexpr (KIND == KIND_CONTIGUOUS) {
+                    // this CTA's block, in the pass of its own group and once per
+                    // block (first column block): a first row out of range
+                    // breaks the layout, and a block whose first row is -1 must
+                    // be all padding (a group id elsewhere in it breaks the
+                    // 128-row alignment contract)
+                    if (ti.own_pass && ti.n_blk == 0 && ti.own_group != -2 &&
+                        !(ti.own_group >= 0 && ti.own_group < p.num_groups)) {
+                        if (ti.own_group != -1) {
+                            if (warp == 0 && lane == 0) record_error(p, DEV_ERR_CHECK, (uint32_t)ti.a_row);
+                        } else if (half == 0) {
+                            const int gid = __ldg(p.m_indices + ti.a_row + r);
+                            if (gid != -1) record_error(p, DEV_ERR_CHECK, (uint32_t)(ti.a_row + r));
+                        }
+                    }
+                }
+                continue;
+            }
+            // which rows of this warp are written
+            bool row_ok;
+            if constexpr (KIND == KIND_CONTIGUOUS) {
+                // the rows of the pass's group (-1 padding rows and the other
+                // block's group stay untouched); in the pass of this CTA's own
+                // block any other valid id breaks the alignment contract
+                const int gid = r < ti.row_limit ? __ldg(p.m_indices + ti.a_row + r) : -1;
+                row_ok = gid == ti.group;
+                if (ti.group == ti.own_group && gid != ti.group && gid != -1 && half == 0)
+                    record_error(p, DEV_ERR_CHECK, (uint32_t)(ti.a_row + r));
+            } else {
+                row_ok = r < ti.row_limit;
+            }
             const int col0 = ti.n_blk * BN + half * COLS;
 
             uint64_t acc2[COLS / 2];
@@ -486,6 +560,11 @@ __global__ void __launch_bounds__(DEFER ? PAIR_DEFER_THREADS : NUM_THREADS, 1)
                                 wait_phase_call(stg_empty_bar, (ep & 1u) ^ 1u, abort_flag, p, ROLE_EPILOGUE)))
                     break;
                 ++ep;
+                // tell the store warp whether this warp's boxes are staged (its
+                // arrival on stg_full below orders this write before the read)
+                if constexpr (!CLIPPED) {
+                    if (lane == 0) staged[warp] = (use_tma && rows_in) ? 1 : 0;
+                }
             }
             if (DEFER && use_tma) {
                 // stage both 64-column boxes; the store warp issues their stores
@@ -588,16 +667,18 @@ __global__ void __launch_bounds__(DEFER ? PAIR_DEFER_THREADS : NUM_THREADS, 1)
         if (lane == 0) {
             uint32_t ep = 0;
             GroupScan scan;
-            for (int t = t_begin; t < num_tiles; t += t_step) {
-                const PairTile ti = get_pair_tile<KIND>(p, t, pblocks, rank, scan);
+            for (int v = v_begin; v < v_end; v = next_v(v)) {
+                const PairTile ti = get_pair_tile<KIND>(p, v, pblocks, rank, scan);
                 if (!ti.valid) continue;
                 if (!wait_phase_call(stg_full_bar, ep & 1u, abort_flag, p, ROLE_EPILOGUE)) break;
                 ++ep;
                 for (int w = 0; w < NUM_EPI_WARPS; ++w) {
                     const int wsub = w & 3, whalf = w >> 2;
-                    const bool rows_in = wsub * 32 < ti.row_limit;
-                    const bool all_rows = CLIPPED || wsub * 32 + 32 <= ti.row_limit;
-                    if (!rows_in || !all_rows) continue;  // nothing staged, or stored row by row
+                    if constexpr (CLIPPED) {
+                        if (wsub * 32 >= ti.row_limit) continue;  // no row of this warp in D
+                    } else {
+                        if (!staged[w]) continue;  // nothing staged: stored row by row, or no row written
+                    }
                     const int d_row = ti.a_row + wsub * 32;
                     for (int bx = 0; bx < COLS / 64; ++bx) {
                         const int x = ti.n_blk * BN + whalf * COLS + bx * 64;

@@ -78,7 +78,7 @@ def test_dense_f32_output_debug_build(debug_lib):
     compare(d_to_bits(d32.to(torch.bfloat16)), ref, what="debug build f32 output")
 
 
-@pytest.mark.parametrize("plan", ["auto", "one_cta_128", "split4_256"])
+@pytest.mark.parametrize("plan", ["auto", "one_cta_128", "split4_256", "pair", "pair_deferred"])
 def test_contiguous_debug_build(debug_lib, plan):
     _plan(debug_lib, plan)
     p = wl.contiguous([130, 0, 256, 77], n=264, k=640, seed=7201)

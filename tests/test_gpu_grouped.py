@@ -168,6 +168,38 @@ def test_masked_pair_tiles(counts, M_cap, pair):
     compare(got[valid], ref[valid], what=f"masked pair={pair} {counts}")
 
 
+@pytest.mark.parametrize("defer", [0, 1])
+@pytest.mark.parametrize("group_rows,n,k", [
+    ([100, 0, 300, 5, 128], 264, 1040),  # odd block counts: pair tiles across two groups
+    ([256, 512, 128], 520, 640),         # groups on 256-row boundaries, the last block alone
+    ([1, 1, 1], 64, 256),                # every pair tile holds two groups (or one and past M)
+    ([513, 77], 2112, 384),              # ragged rows and a partial column block
+    ([128], 256, 128),                   # one block: the second CTA's half past M
+])
+def test_contiguous_pair_tiles(group_rows, n, k, defer):
+    """Contiguous layout on CTA pairs (forced): a pair tile whose two 128-row
+    blocks belong to different groups runs once per group, each pass storing
+    only its group's rows; padding rows stay untouched, the rest within the
+    tolerance of the oracle, with the store warp or the promotion warps
+    storing."""
+    fg.fg_set_config_override(256, 1)
+    fg.fg_set_pair_mode(1)
+    fg.lib().fg_debug_set_pair_defer(defer)
+    try:
+        p = wl.contiguous(group_rows, n=n, k=k, seed=sum(group_rows) + n + k + 7 * defer)
+        assert tuple(fg.fg_query_plan(1, p.M, p.G, n, k)[2:]) == (1, 0, defer)
+        got = d_to_bits(run_contiguous(p))
+    finally:
+        fg.fg_set_config_override(0, 0)
+        fg.fg_set_pair_mode(-1)
+        fg.lib().fg_debug_set_pair_defer(-1)
+    init = np.full((p.M, p.n), SENTINEL, np.uint16)
+    ref, _ = oracle.grouped_contiguous(p.A, 0, p.sA, p.B, 0, p.sB, p.m_indices, init)
+    pad = p.m_indices < 0
+    assert np.array_equal(got[pad], ref[pad]), "padding rows were written"
+    compare(got[~pad], ref[~pad], what=f"contiguous pairs {group_rows} defer={defer}")
+
+
 def run_masked_allow_check(p, expect_check):
     if not expect_check:
         return run_masked(p)

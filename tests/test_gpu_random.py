@@ -42,8 +42,7 @@ def _draw_plan(rng, layout, rows, k):
     if layout in ("dense", "contiguous", "masked") and max_split > 1:
         s = int(rng.integers(2, max_split + 1))
         opts += [(128, s, 0, -1, 0), (256, s, 0, -1, 0)]
-    if layout in ("dense", "masked", "k_grouped"):
-        opts += [(256, 1, 1, 0, 0), (256, 1, 1, 1, 0)]
+    opts += [(256, 1, 1, 0, 0), (256, 1, 1, 1, 0)]
     if layout in ("dense", "masked") and rows <= 256:
         opts += [(0, 0, -1, -1, 1), (0, int(rng.integers(1, max_split + 1)), -1, -1, 1)]
     return opts[int(rng.integers(len(opts)))]
