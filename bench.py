@@ -272,23 +272,26 @@ def graph_us(torch, launch, n_launch):
     return us
 
 
-def quantize_bytes(rows, k):
-    """Algorithmic HBM bytes of one per-token quantization: BF16 X read once,
-    FP8 A and one FP32 scale per row and 128-wide K block written once."""
-    return rows * k * 2 + rows * k + rows * ((k + 127) // 128) * 4
+def quantize_bytes(rows, k, x_bytes=2):
+    """Algorithmic HBM bytes of one per-token quantization: X (BF16, or FP32
+    with x_bytes = 4) read once, FP8 A and one FP32 scale per row and 128-wide
+    K block written once."""
+    return rows * k * x_bytes + rows * k + rows * ((k + 127) // 128) * 4
 
 
-def measure_quantize(fg, torch, dev, stream, hbm_peak, peak_src, reps=20, traffic_tab=None):
+def measure_quantize(fg, torch, dev, stream, hbm_peak, peak_src, reps=20, traffic_tab=None, f32_input=False):
     """Per-token FP8 quantization of the sweep's m = 4096 activations
-    (BF16 [4096][k], k in the sweep), each shape rotating over copies of X, A
-    and sA larger than twice L2; `reps` back-to-back launches between CUDA
-    events on the launching stream, after a warm-up."""
+    (BF16 [4096][k], or FP32 with f32_input, k in the sweep), each shape
+    rotating over copies of X, A and sA larger than twice L2; `reps`
+    back-to-back launches between CUDA events on the launching stream, after a
+    warm-up."""
     ks = sorted({k for (_, k) in wl.DENSE_SWEEP_NK})
     rows_out, tot_b, tot_s = [], 0.0, 0.0
+    xdt = torch.float32 if f32_input else torch.bfloat16
     for k in ks:
         m = max(wl.DENSE_SWEEP_M)
-        x = torch.from_numpy(wl.activations((m, k), seed=wl.seed_for(1, 50 + k % 97))).to(torch.bfloat16).to(dev)
-        nb = quantize_bytes(m, k)
+        x = torch.from_numpy(wl.activations((m, k), seed=wl.seed_for(1, 50 + k % 97))).to(xdt).to(dev)
+        nb = quantize_bytes(m, k, 4 if f32_input else 2)
         ncopy = max(2, -(-ROTATE_BYTES // nb))
         copies = [(x.clone(), torch.empty((m, k), dtype=torch.float8_e4m3fn, device=dev),
                    torch.empty(((k + 127) // 128, fg.fg_scales_a_ld(m)), dtype=torch.float32, device=dev))
@@ -298,7 +301,8 @@ def measure_quantize(fg, torch, dev, stream, hbm_peak, peak_src, reps=20, traffi
             fg.fg_quantize_fp8_per_token(X, A, sA, stream=stream)
         us = graph_us(torch, lambda r, st: fg.fg_quantize_fp8_per_token(*copies[r % ncopy], stream=st), reps)
         rows_out.append({"m": m, "k": k, "us": round(us, 2), "gbs": round(nb / (us * 1e-6) / 1e9, 1),
-                         "algorithmic_bytes": nb, "traffic": (traffic_tab or {}).get((m, 0, k))})
+                         "algorithmic_bytes": nb,
+                         "traffic": None if f32_input else (traffic_tab or {}).get((m, 0, k))})
         tot_b += nb
         tot_s += us * 1e-6
         del copies
@@ -308,9 +312,10 @@ def measure_quantize(fg, torch, dev, stream, hbm_peak, peak_src, reps=20, traffi
     ach = tot_b / tot_s / 1e9
     known = [r["traffic"] for r in rows_out]
     traffic = sum(known) / len(known) if all(v is not None for v in known) else None
-    return {"kernel": "fg::quantize_per_token_kernel<E4M3>",
+    return {"kernel": "fg::quantize_per_token_kernel<E4M3, " + ("FP32" if f32_input else "BF16") + " input>",
             "algorithmic_bytes_per_launch": tot_b / len(rows_out),
-            "workload": "BF16 activations [4096][k] -> FP8 E4M3 A + MN-major 1x128 FP32 scales, k in the sweep",
+            "workload": (("FP32" if f32_input else "BF16") +
+                         " activations [4096][k] -> FP8 E4M3 A + MN-major 1x128 FP32 scales, k in the sweep"),
             "roofline": {"bound": "hbm", "achieved": round(ach, 1), "peak": hbm_peak, "unit": "GB/s",
                          "frac": round(ach / hbm_peak, 3), "traffic": traffic,
                          "peak_source": f"{peak_src}: hbm copy"},
@@ -644,6 +649,7 @@ def run_ours(args, ws, rank, local):
     quant = None
     if not args.no_quantize:
         quant = measure_quantize(fg, torch, dev, stream, hbm_peak, peak_src, traffic_tab=traffic_tab)
+        quant["f32_input"] = measure_quantize(fg, torch, dev, stream, hbm_peak, peak_src, f32_input=True)
 
     # ------------------------------------------------ end to end (host buffers)
     e2e = None

@@ -198,6 +198,15 @@ fg_status fg_scales_a_to_mn_major(const float *src, float *dst, int batches, int
 fg_status fg_quantize_fp8_per_token(const void *X, int ld_x, int fmt, void *A, float *sA, int ld_sA,
                                     const int32_t *masked_m, int batches, int rows, int k, void *stream);
 
+/* fg_quantize_fp8_per_token with FP32 activations: X [batches][rows][ld_x]
+ * float (device), 16-byte aligned, ld_x >= k, ld_x % 4 == 0; finite values.
+ * The same per-group amax, scale and codes, computed on the FP32 values (the
+ * usage walkthrough quantizes FP32 tensors with amax / 448 before the GEMM:
+ * page whose first section is "从一张“算力账单”说起", section 4.2).  Every other
+ * argument, contract and error as above. */
+fg_status fg_quantize_fp8_per_token_f32in(const float *X, int ld_x, int fmt, void *A, float *sA, int ld_sA,
+                                          const int32_t *masked_m, int batches, int rows, int k, void *stream);
+
 /* Smallest valid ld_sA for `rows` rows: rows rounded up to a multiple of 4. */
 int fg_scales_a_ld(int rows);
 

@@ -49,6 +49,7 @@ SIGNATURES = {
     "fg_scales_a_to_mn_major": (_I, [_P, _P, _I, _I, _I, _I, _P]),
     "fg_scales_a_ld": (_I, [_I]),
     "fg_quantize_fp8_per_token": (_I, [_P, _I, _I, _P, _P, _I, _P, _I, _I, _I, _P]),
+    "fg_quantize_fp8_per_token_f32in": (_I, [_P, _I, _I, _P, _P, _I, _P, _I, _I, _I, _P]),
     "fg_get_device_status": (_I, [_P, ctypes.POINTER(_U32)]),
     "fg_set_num_sms": (_I, [_I]),
     "fg_set_watchdog_ms": (_I, [_U32]),
@@ -321,16 +322,17 @@ def fg_scales_a_to_mn_major(src, dst=None, *, stream=None):
 
 
 def fg_quantize_fp8_per_token(X, A=None, sA=None, *, fmt=E4M3, masked_m=None, stream=None):
-    """Per-token (1x128) FP8 quantization of BF16 activations X [rows, k] or
-    [batches, rows, k] into A (same shape, FP8) and MN-major sA [.., kb, ld].
+    """Per-token (1x128) FP8 quantization of BF16 or FP32 activations X
+    [rows, k] or [batches, rows, k] into A (same shape, FP8) and MN-major sA
+    [.., kb, ld] (FP32 X: fg_quantize_fp8_per_token_f32in).
 
     X may be a column slice of a wider matrix (last stride 1, rows ld_x apart,
     batches rows * ld_x apart).  A and sA are allocated when not given (sA with
     ld = fg_scales_a_ld(rows); its padding entries are left unwritten).  With
     masked_m ([batches] int32 on the device) rows r >= masked_m[b] are left
     untouched.  Returns (A, sA)."""
-    if not isinstance(X, torch.Tensor) or not X.is_cuda or X.dtype != torch.bfloat16:
-        raise TypeError("X must be a CUDA bfloat16 tensor")
+    if not isinstance(X, torch.Tensor) or not X.is_cuda or X.dtype not in (torch.bfloat16, torch.float32):
+        raise TypeError("X must be a CUDA bfloat16 or float32 tensor")
     if X.dim() not in (2, 3):
         raise ValueError("X must be [rows, k] or [batches, rows, k]")
     batches = 1 if X.dim() == 2 else X.shape[0]
@@ -362,7 +364,8 @@ def fg_quantize_fp8_per_token(X, A=None, sA=None, *, fmt=E4M3, masked_m=None, st
         if masked_m.shape[0] != batches:
             raise ValueError("masked_m must hold one count per batch")
         mp = masked_m.data_ptr()
-    _launch("fg_quantize_fp8_per_token", (("X", X), ("A", A), ("sA", sA), ("masked_m", masked_m)), stream,
+    name = "fg_quantize_fp8_per_token_f32in" if X.dtype == torch.float32 else "fg_quantize_fp8_per_token"
+    _launch(name, (("X", X), ("A", A), ("sA", sA), ("masked_m", masked_m)), stream,
             X.data_ptr(), ld_x, int(fmt), A.data_ptr(), sA.data_ptr(), sA.shape[-1], mp, batches, rows, k)
     return A, sA
 

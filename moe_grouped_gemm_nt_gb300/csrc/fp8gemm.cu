@@ -467,26 +467,103 @@ fg_status run_kgrouped(const void *A, int a_fmt, const float *sA, int ld_sA, con
 }  // namespace
 
 namespace {
+// The quantization kernel of one FP8 format and input type.
+using QuantKernel = void (*)(const CUtensorMap, fg::QuantParams);
+QuantKernel quantize_kernel(int fmt, int in) {
+    if (in == fg::QUANT_IN_F32)
+        return fmt == FG_E4M3 ? fg::quantize_per_token_kernel<0, fg::QUANT_IN_F32>
+                              : fg::quantize_per_token_kernel<1, fg::QUANT_IN_F32>;
+    return fmt == FG_E4M3 ? fg::quantize_per_token_kernel<0, fg::QUANT_IN_BF16>
+                          : fg::quantize_per_token_kernel<1, fg::QUANT_IN_BF16>;
+}
+
 // Dynamic shared memory attribute of the quantization kernel and its resident
-// CTAs per SM (occupancy query), once per device and format; 0 on failure.
-int quantize_blocks_per_sm(int fmt) {
-    static std::atomic<int> cache[kMaxDevices][2];
+// CTAs per SM (occupancy query), once per device, format and input type; 0 on
+// failure.
+int quantize_blocks_per_sm(int fmt, int in) {
+    static std::atomic<int> cache[kMaxDevices][2][2];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
-    const int v = cache[dev][fmt].load();
+    const int v = cache[dev][fmt][in].load();
     if (v > 0) return v;
-    auto kernel = fmt == FG_E4M3 ? fg::quantize_per_token_kernel<0> : fg::quantize_per_token_kernel<1>;
+    const QuantKernel kernel = quantize_kernel(fmt, in);
+    const int smem = fg::quant_smem_bytes(in);
     int n = 0;
-    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, fg::QUANT_SMEM_BYTES) !=
-            cudaSuccess ||
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, fg::QUANT_THREADS, fg::QUANT_SMEM_BYTES) !=
-            cudaSuccess ||
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, fg::QUANT_THREADS, smem) != cudaSuccess ||
         n <= 0) {
         cudaGetLastError();
         return 0;
     }
-    cache[dev][fmt].store(n);
+    cache[dev][fmt][in].store(n);
     return n;
+}
+
+// Shared part of the quantization entry points; `in`: element type of X.
+fg_status quantize(int in, const void *X, int ld_x, int fmt, void *A, float *sA, int ld_sA, const int32_t *masked_m,
+                   int batches, int rows, int k, void *stream) {
+    if (!X || !A || !sA || batches < 1 || rows < 0 || k < 1 || ld_x < k || ld_sA < rows || ld_sA < 1)
+        return FG_ERR_INVALID_ARG;
+    if (fmt != FG_E4M3 && fmt != FG_E5M2) return FG_ERR_INVALID_ARG;
+    const int esize = in == fg::QUANT_IN_F32 ? 4 : 2;
+    if (!aligned16(X) || !aligned16(A) || !aligned16(sA) || (ld_x * esize) % 16 != 0 || ld_sA % 4 != 0)
+        return FG_ERR_MISALIGNED;
+    if (k % 16 != 0) return FG_ERR_UNSUPPORTED;
+    const int kb = cdiv(k, 128);
+    if (kb > 65535 || batches > 65535) return FG_ERR_UNSUPPORTED;
+    if (rows == 0) return FG_OK;
+    const long long units = (long long)batches * cdiv(rows, fg::QUANT_ROWS) * kb;
+    if (units > 0x7FFFFFFFLL - (1LL << 20)) return FG_ERR_UNSUPPORTED;  // unit index + grid stays in int
+    DeviceInfo *dev = nullptr;
+    if (fg_status st = device_info(&dev); st != FG_OK) return st;
+    const int per_sm = quantize_blocks_per_sm(fmt, in);
+    if (per_sm <= 0) return cuda_fail();
+    int sms = dev->num_sms;
+    const int ovr = g_num_sms_override.load();
+    if (ovr > 0 && ovr < sms) sms = ovr;
+
+    fg::QuantParams p{};
+    p.x = X;
+    p.a = static_cast<uint8_t *>(A);
+    p.sa = sA;
+    p.masked_m = masked_m;
+    p.status = dev->status;
+    p.ld_x = ld_x;
+    p.ld_sa = ld_sA;
+    p.rows = rows;
+    p.k = k;
+    p.kb = kb;
+    p.timeout_ns = (unsigned long long)g_watchdog_ms.load() * 1000000ull;
+    p.debug_skip_unit = g_debug_skip_iter.exchange(-1);
+    p.row_blocks = cdiv(rows, fg::QUANT_ROWS);
+    p.units = (int)units;
+
+    // persistent CTAs: as many as are resident at once, each walks the units
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3((unsigned)std::min<long long>(units, (long long)sms * per_sm), 1, 1);
+    cfg.blockDim = dim3(fg::QUANT_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = fg::quant_smem_bytes(in);
+    cfg.stream = static_cast<cudaStream_t>(stream);
+    cudaLaunchAttribute at[1];
+    if (g_pdl.load() != 0) {
+        at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        at[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = at;
+        cfg.numAttrs = 1;
+    }
+    // X as a 3-D tensor {k, rows, batches}; one box = one unit (128 columns x 32 rows)
+    CUtensorMap tx;
+    {
+        const uint64_t dims[3] = {(uint64_t)k, (uint64_t)rows, (uint64_t)batches};
+        const uint64_t strides[2] = {(uint64_t)ld_x * esize, (uint64_t)ld_x * esize * (uint64_t)rows};
+        const uint32_t box[3] = {128, (uint32_t)fg::QUANT_ROWS, 1};
+        if (!encode(&tx, in == fg::QUANT_IN_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, X,
+                    3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE))
+            return cuda_fail();
+    }
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, quantize_kernel(fmt, in), tx, p);
+    if (e != cudaSuccess) return cuda_fail();
+    return cudaPeekAtLastError() == cudaSuccess ? FG_OK : cuda_fail();
 }
 }  // namespace
 
@@ -559,67 +636,12 @@ fg_status fg_scales_a_to_mn_major(const float *src, float *dst, int batches, int
 
 fg_status fg_quantize_fp8_per_token(const void *X, int ld_x, int fmt, void *A, float *sA, int ld_sA,
                                     const int32_t *masked_m, int batches, int rows, int k, void *stream) {
-    if (!X || !A || !sA || batches < 1 || rows < 0 || k < 1 || ld_x < k || ld_sA < rows || ld_sA < 1)
-        return FG_ERR_INVALID_ARG;
-    if (fmt != FG_E4M3 && fmt != FG_E5M2) return FG_ERR_INVALID_ARG;
-    if (!aligned16(X) || !aligned16(A) || !aligned16(sA) || ld_x % 8 != 0 || ld_sA % 4 != 0)
-        return FG_ERR_MISALIGNED;
-    if (k % 16 != 0) return FG_ERR_UNSUPPORTED;
-    const int kb = cdiv(k, 128);
-    if (kb > 65535 || batches > 65535) return FG_ERR_UNSUPPORTED;
-    if (rows == 0) return FG_OK;
-    const long long units = (long long)batches * cdiv(rows, fg::QUANT_ROWS) * kb;
-    if (units > 0x7FFFFFFFLL - (1LL << 20)) return FG_ERR_UNSUPPORTED;  // unit index + grid stays in int
-    DeviceInfo *dev = nullptr;
-    if (fg_status st = device_info(&dev); st != FG_OK) return st;
-    const int per_sm = quantize_blocks_per_sm(fmt);
-    if (per_sm <= 0) return cuda_fail();
-    int sms = dev->num_sms;
-    const int ovr = g_num_sms_override.load();
-    if (ovr > 0 && ovr < sms) sms = ovr;
+    return quantize(fg::QUANT_IN_BF16, X, ld_x, fmt, A, sA, ld_sA, masked_m, batches, rows, k, stream);
+}
 
-    fg::QuantParams p{};
-    p.x = static_cast<const uint16_t *>(X);
-    p.a = static_cast<uint8_t *>(A);
-    p.sa = sA;
-    p.masked_m = masked_m;
-    p.status = dev->status;
-    p.ld_x = ld_x;
-    p.ld_sa = ld_sA;
-    p.rows = rows;
-    p.k = k;
-    p.kb = kb;
-    p.timeout_ns = (unsigned long long)g_watchdog_ms.load() * 1000000ull;
-    p.debug_skip_unit = g_debug_skip_iter.exchange(-1);
-    p.row_blocks = cdiv(rows, fg::QUANT_ROWS);
-    p.units = (int)units;
-
-    // persistent CTAs: as many as are resident at once, each walks the units
-    cudaLaunchConfig_t cfg{};
-    cfg.gridDim = dim3((unsigned)std::min<long long>(units, (long long)sms * per_sm), 1, 1);
-    cfg.blockDim = dim3(fg::QUANT_THREADS, 1, 1);
-    cfg.dynamicSmemBytes = fg::QUANT_SMEM_BYTES;
-    cfg.stream = static_cast<cudaStream_t>(stream);
-    cudaLaunchAttribute at[1];
-    if (g_pdl.load() != 0) {
-        at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        at[0].val.programmaticStreamSerializationAllowed = 1;
-        cfg.attrs = at;
-        cfg.numAttrs = 1;
-    }
-    // X as a 3-D tensor {k, rows, batches}; one box = one unit (128 columns x 64 rows)
-    CUtensorMap tx;
-    {
-        const uint64_t dims[3] = {(uint64_t)k, (uint64_t)rows, (uint64_t)batches};
-        const uint64_t strides[2] = {(uint64_t)ld_x * 2, (uint64_t)ld_x * 2 * (uint64_t)rows};
-        const uint32_t box[3] = {128, (uint32_t)fg::QUANT_ROWS, 1};
-        if (!encode(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, X, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE))
-            return cuda_fail();
-    }
-    const cudaError_t e = fmt == FG_E4M3 ? cudaLaunchKernelEx(&cfg, fg::quantize_per_token_kernel<0>, tx, p)
-                                         : cudaLaunchKernelEx(&cfg, fg::quantize_per_token_kernel<1>, tx, p);
-    if (e != cudaSuccess) return cuda_fail();
-    return cudaPeekAtLastError() == cudaSuccess ? FG_OK : cuda_fail();
+fg_status fg_quantize_fp8_per_token_f32in(const float *X, int ld_x, int fmt, void *A, float *sA, int ld_sA,
+                                          const int32_t *masked_m, int batches, int rows, int k, void *stream) {
+    return quantize(fg::QUANT_IN_F32, X, ld_x, fmt, A, sA, ld_sA, masked_m, batches, rows, k, stream);
 }
 
 int fg_scales_a_ld(int rows) { return rows <= 0 ? 4 : (rows + 3) / 4 * 4; }

@@ -1,4 +1,4 @@
-// quantize_kernel.cuh -- per-token (1 x 128) FP8 quantization of BF16
+// quantize_kernel.cuh -- per-token (1 x 128) FP8 quantization of BF16 or FP32
 // activations into the GEMM's LHS: the FP8 matrix A and its MN-major scales sA.
 //
 // What it computes (page "DeepSeek开源周第三天DeepGEMM", section "基本用法": the
@@ -13,9 +13,9 @@
 // with fmax = 448 (E4M3) or 57344 (E5M2), IEEE float32 division for both
 // quotients, and round-to-nearest-even, saturating conversion to FP8.
 //
-// The work is bound by HBM bandwidth: 2 bytes read and 1 + 4/128 bytes written
-// per element.  A unit of work is 32 rows x one 128-column K block (8 KB of
-// X).  CTAs are persistent (as many as fit on the SMs: seven per SM, by registers);
+// The work is bound by HBM bandwidth: 2 bytes (FP32 input: 4) read and
+// 1 + 4/128 bytes written per element.  A unit of work is 32 rows x one
+// 128-column K block (8 KB of BF16 X, 16 KB of FP32).  CTAs are persistent (as many as fit on the SMs: seven per SM, by registers);
 // each takes a contiguous range of units, walked along K.  One producer
 // thread loads each unit with a single 3-D TMA box (columns past k and rows
 // past the batch read as zeros) into the CTA's shared-memory stage; four
@@ -25,9 +25,11 @@
 // slower: more small CTAs per SM keep HBM busier than deeper rings.)  Each
 // row is handled by 4 consecutive lanes with 32 columns each (four 16-byte
 // chunks; odd rows take the chunks in the other order, so every quarter-
-// warp's shared loads hit 32 distinct banks); the group maximum runs on BF16
-// pairs (max.xorsign.abs: the larger magnitude of each half) and needs two
-// butterfly shuffles.  A consumer warp writes its codes (8-byte stores, 32
+// warp's shared loads hit 32 distinct banks; FP32 rows are 512 bytes, so odd
+// rows instead read the two 16-byte halves of each 32-byte piece in the other
+// order); the group maximum runs on BF16 pairs (max.xorsign.abs: the larger
+// magnitude of each half) or on FP32 magnitudes and needs two butterfly
+// shuffles.  A consumer warp writes its codes (8-byte stores, 32
 // contiguous bytes per row and store) and the row's scale (8 rows of a warp:
 // 32 contiguous bytes of sA).  Every wait is bounded by a %globaltimer
 // watchdog: on expiry the CTA records FG_ERR_TIMEOUT, stops, and waits (again
@@ -63,7 +65,7 @@
 namespace fg {
 
 struct QuantParams {
-    const uint16_t *x;         // bfloat16 bits [batches][rows][ld_x]
+    const void *x;             // bfloat16 bits or float32 [batches][rows][ld_x]
     uint8_t *a;                // FP8 codes [batches][rows][k]
     float *sa;                 // [batches][kb][ld_sa]
     const int32_t *masked_m;   // [batches] valid rows per batch, or null (all rows)
@@ -83,8 +85,12 @@ constexpr int QUANT_ROWS = 32;                              // rows per unit
 constexpr int QUANT_CONSUMER_WARPS = QUANT_ROWS / 8;        // 8 rows each, 4 lanes per row
 constexpr int QUANT_THREADS = (QUANT_CONSUMER_WARPS + 1) * 32;  // + the producer warp
 constexpr int QUANT_STAGES = 1;  // measured best: many small CTAs beat deep rings
-constexpr int QUANT_STAGE_BYTES = QUANT_ROWS * 128 * 2;     // 8 KB of BF16
-constexpr int QUANT_SMEM_BYTES = QUANT_STAGES * QUANT_STAGE_BYTES + 2 * QUANT_STAGES * 8 + 16;
+constexpr int QUANT_IN_BF16 = 0, QUANT_IN_F32 = 1;  // element type of X
+// one unit of X: 8 KB of BF16 or 16 KB of FP32
+__host__ __device__ constexpr int quant_stage_bytes(int in) { return QUANT_ROWS * 128 * (in == QUANT_IN_F32 ? 4 : 2); }
+__host__ __device__ constexpr int quant_smem_bytes(int in) {
+    return QUANT_STAGES * quant_stage_bytes(in) + 2 * QUANT_STAGES * 8 + 16;
+}
 constexpr float QUANT_MIN_FAST_SCALE = 0x1p-40f;
 constexpr float QUANT_MIN_FAST_AMAX = 0x1p-100f;
 constexpr uint32_t QUANT_ROLE_PRODUCER = 1, QUANT_ROLE_CONSUMER = 3;
@@ -211,9 +217,10 @@ __device__ __forceinline__ uint64_t bf16x2_to_f32x2(uint32_t w) {
     return f32x2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
 }
 
-template <int FMT>
+template <int FMT, int IN>
 __global__ void __launch_bounds__(QUANT_THREADS)
     quantize_per_token_kernel(const __grid_constant__ CUtensorMap tmap_x, QuantParams p) {
+    constexpr int QUANT_STAGE_BYTES = quant_stage_bytes(IN);
     extern __shared__ __align__(1024) uint8_t smem[];
     const uint32_t sbase = smem_u32(smem);
     const uint32_t full0 = sbase + QUANT_STAGES * QUANT_STAGE_BYTES;  // full[s] = full0 + 8 s
@@ -295,23 +302,53 @@ __global__ void __launch_bounds__(QUANT_THREADS)
         if (!__all_sync(0xffffffffu, ok)) break;  // warp-uniform exit
         const int row = w.rb * QUANT_ROWS + lrow;
         const bool act_row = row < w.limit;
-        uint32_t wd[16];  // BF16 pairs: chunk c in wd[4c .. 4c+3]
-        const uint8_t *srow = smem + s * QUANT_STAGE_BYTES + lrow * 256 + 16 * jq;
+        // this lane's 32 values (columns 32 c' + 8 jq .. + 7 of chunks c = 0..3):
+        // BF16 pairs wd[4c .. 4c+3], or FP32 xf[8c .. 8c+7]
+        uint32_t wd[IN == QUANT_IN_F32 ? 1 : 16];
+        float xf[IN == QUANT_IN_F32 ? 32 : 1];
+        if constexpr (IN == QUANT_IN_F32) {
+            const uint8_t *srow = smem + s * QUANT_STAGE_BYTES + lrow * 512 + 32 * jq;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            const uint4 v = *reinterpret_cast<const uint4 *>(srow + 64 * (c ^ flip));
-            wd[4 * c] = v.x;
-            wd[4 * c + 1] = v.y;
-            wd[4 * c + 2] = v.z;
-            wd[4 * c + 3] = v.w;
+            for (int c = 0; c < 4; ++c) {
+                // odd rows take the second 16 bytes first: the quarter-warp's two
+                // rows then cover all 32 banks in each load
+                const float4 v0 = *reinterpret_cast<const float4 *>(srow + 128 * (c ^ flip) + 16 * flip);
+                const float4 v1 = *reinterpret_cast<const float4 *>(srow + 128 * (c ^ flip) + 16 * (flip ^ 1));
+                const float4 lo = flip ? v1 : v0, hi = flip ? v0 : v1;
+                xf[8 * c] = lo.x;
+                xf[8 * c + 1] = lo.y;
+                xf[8 * c + 2] = lo.z;
+                xf[8 * c + 3] = lo.w;
+                xf[8 * c + 4] = hi.x;
+                xf[8 * c + 5] = hi.y;
+                xf[8 * c + 6] = hi.z;
+                xf[8 * c + 7] = hi.w;
+            }
+        } else {
+            const uint8_t *srow = smem + s * QUANT_STAGE_BYTES + lrow * 256 + 16 * jq;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const uint4 v = *reinterpret_cast<const uint4 *>(srow + 64 * (c ^ flip));
+                wd[4 * c] = v.x;
+                wd[4 * c + 1] = v.y;
+                wd[4 * c + 2] = v.z;
+                wd[4 * c + 3] = v.w;
+            }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(empty0 + 8 * s);  // the stage may be refilled now
 
-        uint32_t m2 = 0u;
+        float amax;
+        if constexpr (IN == QUANT_IN_F32) {
+            amax = 0.f;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) m2 = bf16x2_max_abs(m2, wd[i]);
-        float amax = fmaxf(__uint_as_float((m2 << 16) & 0x7FFFFFFFu), __uint_as_float(m2 & 0x7FFF0000u));
+            for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(xf[i]));
+        } else {
+            uint32_t m2 = 0u;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) m2 = bf16x2_max_abs(m2, wd[i]);
+            amax = fmaxf(__uint_as_float((m2 << 16) & 0x7FFFFFFFu), __uint_as_float(m2 & 0x7FFF0000u));
+        }
         // the 4 lanes of a row are 4 consecutive lanes: xor 1, 2 stays inside them
         amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
         amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
@@ -328,7 +365,11 @@ __global__ void __launch_bounds__(QUANT_THREADS)
                 uint32_t half[2];
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
-                    const uint64_t x2 = bf16x2_to_f32x2(wd[2 * i + h]);
+                    uint64_t x2;
+                    if constexpr (IN == QUANT_IN_F32)
+                        x2 = f32x2(xf[4 * i + 2 * h], xf[4 * i + 2 * h + 1]);
+                    else
+                        x2 = bf16x2_to_f32x2(wd[2 * i + h]);
                     uint64_t q = f32x2_mul(x2, ny2);
                     q = f32x2_fma(f32x2_fma(q, s2, x2), ny2, q);
                     q = f32x2_fma(f32x2_fma(q, s2, x2), ny2, q);
@@ -344,9 +385,15 @@ __global__ void __launch_bounds__(QUANT_THREADS)
                 uint32_t half[2];
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
-                    const uint32_t wv = wd[2 * i + h];
-                    half[h] = cvt_fp8x2<FMT>(__fdiv_rn(-__uint_as_float(wv << 16), scale),
-                                             __fdiv_rn(-__uint_as_float(wv & 0xFFFF0000u), scale));
+                    float x0, x1;
+                    if constexpr (IN == QUANT_IN_F32) {
+                        x0 = xf[4 * i + 2 * h];
+                        x1 = xf[4 * i + 2 * h + 1];
+                    } else {
+                        x0 = __uint_as_float(wd[2 * i + h] << 16);
+                        x1 = __uint_as_float(wd[2 * i + h] & 0xFFFF0000u);
+                    }
+                    half[h] = cvt_fp8x2<FMT>(__fdiv_rn(-x0, scale), __fdiv_rn(-x1, scale));
                 }
                 codes[i] = half[0] | (half[1] << 16);
             }

@@ -26,23 +26,24 @@ A_SENTINEL = 0x7F
 SA_SENTINEL_BITS = 0x7FCADBAD  # a quiet-NaN pattern no scale can take (filled through an int32 view)
 
 
-def _x_device(x, ld_x=None):
-    """float32 (bfloat16-valued) [.., rows, k] -> CUDA bfloat16 with row pitch ld_x."""
+def _x_device(x, ld_x=None, dtype=torch.bfloat16):
+    """float32 [.., rows, k] (bfloat16-valued for a bfloat16 X) -> CUDA tensor of
+    `dtype` with row pitch ld_x."""
     *lead, rows, k = x.shape
     ld_x = k if ld_x is None else ld_x
     full = np.zeros((*lead, rows, ld_x), np.float32)
     full[..., :k] = x
     if ld_x > k:
         full[..., k:] = 1.0e30  # columns past k must not reach any group maximum
-    t = torch.from_numpy(full).to(torch.bfloat16).cuda()
+    t = torch.from_numpy(full).to(dtype).cuda()
     return t[..., :k]
 
 
-def _run(x, fmt, ld_x=None, masked_m=None, ld_sa=None):
+def _run(x, fmt, ld_x=None, masked_m=None, ld_sa=None, dtype=torch.bfloat16):
     *lead, rows, k = x.shape
     kb = (k + 127) // 128
     ld_sa = fg.fg_scales_a_ld(rows) if ld_sa is None else ld_sa
-    X = _x_device(x, ld_x)
+    X = _x_device(x, ld_x, dtype)
     A = torch.full((*lead, rows, k), A_SENTINEL, dtype=torch.uint8, device="cuda")
     sA = torch.full((*lead, kb, ld_sa), SA_SENTINEL_BITS, dtype=torch.int32, device="cuda").view(torch.float32)
     mm = None if masked_m is None else torch.tensor(masked_m, dtype=torch.int32, device="cuda")
@@ -261,3 +262,95 @@ def test_quantize_exact_ties(fmt):
     x = np.stack(rows).astype(np.float32)
     A, sA = _run(x, fmt)
     _check_against_oracle(x, fmt, A, sA)
+
+
+# ------------------------------------------------------------ FP32 activations
+# fg_quantize_fp8_per_token_f32in: the same contract on float32 X, whose values
+# carry full 24-bit significands and reach the float32 extremes.
+
+def _f32_activations(shape, seed):
+    """Seeded float32 activations that are not bfloat16 values (random low
+    significand bits), with the magnitude mix of the BF16 workload."""
+    x = wl.activations(shape, seed=seed).astype(np.float32)
+    jitter = wl.rng_for(seed + 1).uniform(-1, 1, size=x.shape).astype(np.float32)
+    return (x * (np.float32(1) + jitter * np.float32(2.0 ** -9))).astype(np.float32)
+
+
+@pytest.mark.parametrize("fmt", [wl.E4M3, wl.E5M2])
+@pytest.mark.parametrize("batches,rows,k,ld_x", [
+    (1, 1, 16, 16),
+    (1, 31, 112, 116),      # one partial K block, a row pitch of 116 floats
+    (1, 33, 144, 160),
+    (1, 257, 304, 304),
+    (3, 70, 256, 260),      # batches
+    (2, 1, 128, 132),       # one row per batch
+])
+def test_quantize_f32_input_bit_exact(fmt, batches, rows, k, ld_x):
+    x = _f32_activations((batches, rows, k), seed=rows * 11 + k + fmt)
+    assert not np.array_equal(x, torch.from_numpy(x).to(torch.bfloat16).to(torch.float32).numpy())
+    A, sA = _run(x, fmt, ld_x=ld_x, dtype=torch.float32)
+    _check_against_oracle(x, fmt, A, sA)
+
+
+@pytest.mark.parametrize("fmt", [wl.E4M3, wl.E5M2])
+def test_quantize_f32_input_extremes(fmt):
+    """Zero groups, signed zeros, the largest float32 values (scale amax / fmax
+    stays finite), float32 subnormals down to 2^-149 (scales in the subnormal
+    range: the IEEE-division fallback), magnitudes log-uniform over the whole
+    float32 range, and quotients on exact FP8 midpoints of full-precision
+    scales."""
+    rng = wl.rng_for(4040 + fmt)
+    rows, k = 64, 512
+    ceil = rng.uniform(-149, 127, size=(rows, k // 128, 1))
+    e = ceil - rng.uniform(0, 40, size=(rows, k // 128, 128))
+    x = (np.exp2(np.maximum(e, -149)) * rng.choice([-1.0, 1.0], size=e.shape)).reshape(rows, k).astype(np.float32)
+    fmax32 = np.float32(np.finfo(np.float32).max)
+    x[0] = 0.0
+    x[1] = -0.0
+    x[2, :] = fmax32
+    x[2, 1::2] = -fmax32
+    x[3, :] = np.float32(2.0 ** -149)
+    x[3, 7] = np.float32(5 * 2.0 ** -149)
+    # quotients on FP8 midpoints: x = mid * s with scales of 19 significant
+    # bits whose reciprocals are inexact (mid has at most 5, fmax 3 bits, so
+    # mid * s and amax = fmax * s are exact float32 values and amax / fmax = s)
+    t = oracle.decode_table(fmt)
+    fm = 448.0 if fmt == wl.E4M3 else 57344.0
+    vals = sorted({float(v) for v in t[:128] if np.isfinite(v) and v >= 0})
+    mids = np.array([(a + b) / 2 for a, b in zip(vals[:-1], vals[1:])], np.float64)
+    for i, sc in enumerate([1.0 + 2.0 ** -18, 3.0 * (1 - 2.0 ** -17), (2.0 ** 19 - 1) * 2.0 ** -25]):
+        row = np.resize(mids, 128) * sc
+        row[0] = fm * sc  # the group maximum
+        assert np.all(row.astype(np.float32).astype(np.float64) == row)
+        x[4 + i, :128] = row.astype(np.float32)
+    A, sA = _run(x, fmt, dtype=torch.float32)
+    _check_against_oracle(x, fmt, A, sA)
+
+
+def test_quantize_f32_input_masked_counts():
+    x = _f32_activations((4, 96, 512), seed=81)
+    counts = [0, 96, 33, 1]
+    A, sA = _run(x, wl.E5M2, masked_m=counts, dtype=torch.float32)
+    _check_against_oracle(x, wl.E5M2, A, sA, limits=counts)
+    assert fg.fg_get_device_status()[0] == fg.FG_OK
+
+
+@pytest.mark.parametrize("rows,k", [(4096, 7168), (64, 2048)])
+def test_quantize_f32_input_full_size_bit_exact(rows, k):
+    x = _f32_activations((rows, k), seed=rows + k + 3)
+    A, sA = _run(x, wl.E4M3, dtype=torch.float32)
+    _check_against_oracle(x, wl.E4M3, A, sA)
+
+
+def test_quantize_f32_input_then_gemm_matches_oracle():
+    m, n, k = 300, 512, 640
+    x = _f32_activations((m, k), seed=82)
+    pb = wl.dense(8, n, k, seed=83)  # only its B and sB are used
+    A, sA = fg.fg_quantize_fp8_per_token(_x_device(x, dtype=torch.float32), fmt=wl.E4M3)
+    D = torch.empty((m, n), dtype=torch.bfloat16, device="cuda")
+    fg.fg_gemm_fp8_nt(A, sA, dev(pb.B, fp8_dtype(pb.b_fmt)), dev(pb.sB), D)
+    torch.cuda.synchronize()
+    q, s = oracle.quantize_per_token(x, wl.E4M3)
+    ref, _ = oracle.gemm_fp8_nt(q, wl.E4M3, s, pb.B, pb.b_fmt, pb.sB)
+    compare(d_to_bits(D), ref, what="quantize (FP32 input) + dense GEMM")
+
