@@ -18,6 +18,7 @@ SENT32 = 0x7FCADBAD  # float32 NaN pattern the kernels never write
 
 
 def reset_knobs():
+    fg.fg_set_num_sms(0)
     fg.fg_set_config_override(0, 0)
     fg.fg_set_pair_mode(-1)
     fg.fg_set_swap_mode(-1)
@@ -37,8 +38,9 @@ def _draw_plan(rng, layout, rows, k):
     return opts[int(rng.integers(len(opts)))]
 
 
-def _apply(plan):
+def _apply(plan, sms):
     bn, split, pair, defer, swap = plan
+    fg.fg_set_num_sms(sms)
     fg.fg_set_config_override(bn, split)
     fg.fg_set_pair_mode(pair)
     fg.lib().fg_debug_set_pair_defer(defer)
@@ -82,6 +84,9 @@ def random_case(case, rng_base, seed_base):
     f32 = bool(rng.random() < 0.3)
     n = 8 * int(rng.integers(1, 161))
     seed = wl.seed_for(9, seed_base + case)
+    # persistent CTAs: all SMs, or few, so that each CTA (or CTA pair) walks many
+    # tiles of the ragged problem and carries its rings and scans across them
+    sms = int(rng.choice([0, 0, 2, 3, 8]))
     sfx = "_f32out" if f32 else ""
 
     if layout == "dense":
@@ -89,7 +94,7 @@ def random_case(case, rng_base, seed_base):
         a_fmt = wl.E5M2 if rng.random() < 0.2 else wl.E4M3
         p = wl.dense(m, n, k, seed=seed, b_fmt=b_fmt, a_fmt=a_fmt)
         plan = _draw_plan(rng, layout, m, k)
-        _apply(plan)
+        _apply(plan, sms)
         D = _empty((m, n), f32)
         getattr(fg, "fg_gemm_fp8_nt" + sfx)(dev(p.A, fp8_dtype(a_fmt)), fg.fg_scales_a_to_mn_major(dev(p.sA)),
                                             dev(p.B, fp8_dtype(b_fmt)), dev(p.sB), D)
@@ -103,7 +108,7 @@ def random_case(case, rng_base, seed_base):
         if p.M == 0:
             return False
         plan = _draw_plan(rng, layout, p.M, k)
-        _apply(plan)
+        _apply(plan, sms)
         D = _empty((p.M, n), f32)
         getattr(fg, "fg_grouped_gemm_fp8_contiguous" + sfx)(
             dev(p.A, fp8_dtype(p.a_fmt)), fg.fg_scales_a_to_mn_major(dev(p.sA)), dev(p.B, fp8_dtype(b_fmt)),
@@ -118,7 +123,7 @@ def random_case(case, rng_base, seed_base):
         counts = [int(rng.choice([0, M_cap, int(rng.integers(0, M_cap + 1))])) for _ in range(G)]
         p = wl.masked(G, M_cap, n=n, k=k, seed=seed, masked_m=counts, b_fmt=b_fmt)
         plan = _draw_plan(rng, layout, M_cap, k)
-        _apply(plan)
+        _apply(plan, sms)
         D = _empty((G, M_cap, n), f32)
         getattr(fg, "fg_grouped_gemm_fp8_masked" + sfx)(
             dev(p.A, fp8_dtype(p.a_fmt)), fg.fg_scales_a_to_mn_major(dev(p.sA)), dev(p.B, fp8_dtype(b_fmt)),
@@ -132,7 +137,7 @@ def random_case(case, rng_base, seed_base):
         K = sum(ks) + 16 * int(rng.integers(0 if sum(ks) else 1, 11))
         p = wl.k_grouped(M, n, ks, seed=seed, b_fmt=b_fmt, K=K)
         plan = _draw_plan(rng, layout, M, K)
-        _apply(plan)
+        _apply(plan, sms)
         D = _empty((G, M, n), f32)
         getattr(fg, "fg_k_grouped_gemm_fp8_nt" + sfx)(
             dev(p.A, fp8_dtype(p.a_fmt)), fg.fg_scales_a_to_mn_major(dev(p.sA)), dev(p.B, fp8_dtype(b_fmt)),
@@ -141,6 +146,7 @@ def random_case(case, rng_base, seed_base):
         written = np.ones((G, M, n), bool)
     torch.cuda.synchronize()
     check_status()
-    what = f"case {case}: {layout} {tuple(D.shape)} k={p.k} B fmt {b_fmt} {'f32' if f32 else 'bf16'} plan {plan}"
+    what = (f"case {case}: {layout} {tuple(D.shape)} k={p.k} B fmt {b_fmt} {'f32' if f32 else 'bf16'} plan {plan} "
+            f"sms {sms}")
     _check(D, f32, ref16, ref64, written, what)
     return True
