@@ -342,6 +342,46 @@ def test_quantize_f32_input_full_size_bit_exact(rows, k):
     _check_against_oracle(x, wl.E4M3, A, sA)
 
 
+def test_graph_replays_f32_quantize_and_masked_gemm_with_new_counts():
+    """FP32-input quantize + masked GEMM captured once in a CUDA graph and
+    replayed with new device-side counts."""
+    G, M_cap, n, k = 2, 256, 264, 384
+    x = _f32_activations((G, M_cap, k), seed=84)
+    pb = wl.masked(G, M_cap, n=n, k=k, seed=85)  # its B and sB
+    X = _x_device(x, dtype=torch.float32)
+    A = torch.empty((G, M_cap, k), dtype=torch.float8_e4m3fn, device="cuda")
+    sA = torch.empty((G, (k + 127) // 128, fg.fg_scales_a_ld(M_cap)), dtype=torch.float32, device="cuda")
+    B, sB = dev(pb.B, fp8_dtype(pb.b_fmt)), dev(pb.sB)
+    counts = torch.zeros(G, dtype=torch.int32, device="cuda")
+    D = torch.empty((G, M_cap, n), dtype=torch.bfloat16, device="cuda")
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        fg.fg_quantize_fp8_per_token(X, A, sA, fmt=wl.E4M3, masked_m=counts, stream=s)
+        fg.fg_grouped_gemm_fp8_masked(A, sA, B, sB, D, counts, stream=s)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            fg.fg_quantize_fp8_per_token(X, A, sA, fmt=wl.E4M3, masked_m=counts, stream=s)
+            fg.fg_grouped_gemm_fp8_masked(A, sA, B, sB, D, counts, stream=s)
+    torch.cuda.current_stream().wait_stream(s)
+    q, sc = oracle.quantize_per_token(x, wl.E4M3)
+    for cnt in ([256, 7], [0, 129]):
+        D.view(torch.int16).fill_(int(np.array(SENTINEL, np.uint16).view(np.int16)))
+        counts.copy_(torch.tensor(cnt, dtype=torch.int32))
+        g.replay()
+        torch.cuda.synchronize()
+        got = d_to_bits(D)
+        init = np.full((G, M_cap, n), SENTINEL, np.uint16)
+        ref, _ = oracle.grouped_masked(q, wl.E4M3, sc, pb.B, pb.b_fmt, pb.sB, np.array(cnt, np.int32), init)
+        for gi in range(G):
+            c = cnt[gi]
+            assert np.all(got[gi, c:] == SENTINEL)
+            if c:
+                compare(got[gi, :c], ref[gi, :c], what=f"FP32 quantize graph replay group {gi}")
+    assert fg.fg_get_device_status()[0] == fg.FG_OK
+
+
 def test_quantize_f32_input_then_gemm_matches_oracle():
     m, n, k = 300, 512, 640
     x = _f32_activations((m, k), seed=82)

@@ -65,13 +65,14 @@ def test_status_is_cleared_by_reading():
     assert st == fg.FG_OK
 
 
+@pytest.mark.parametrize("x_dtype", [torch.bfloat16, torch.float32])
 @pytest.mark.parametrize("skip_unit", [0, 5])
-def test_quantizer_unfilled_stage_times_out_and_context_survives(skip_unit):
+def test_quantizer_unfilled_stage_times_out_and_context_survives(skip_unit, x_dtype):
     """The quantizer's producer leaves one unit unfilled in every CTA: the
     consumers' bounded wait expires, the CTA drains the copies it issued and
-    returns, and the next call is bit-exact."""
+    returns, and the next call is bit-exact (BF16 and FP32 input)."""
     x = wl.activations((4096, 1024), seed=91)  # 1024 units of 32 rows x 128 columns
-    X = torch.from_numpy(x).to(torch.bfloat16).cuda()
+    X = torch.from_numpy(x).to(x_dtype).cuda()
     fg.fg_set_watchdog_ms(200)
     fg.fg_set_num_sms(4)  # a few persistent CTAs, each with many units
     try:
