@@ -3,8 +3,9 @@ parity sweeps of the release library and of the FG_DEBUG build: each draw
 picks the shape (ragged in every dimension), the FP8 format of B (and of A for
 dense calls), the output type and a tile plan forced through the process-wide
 knobs, runs the call through the C ABI and compares every output element with
-the CPU oracle; grouped calls start from a sentinel-filled D and the rows they
-must leave untouched are checked bit for bit."""
+the CPU oracle; D starts filled with a sentinel inside a buffer with sentinel
+guard bands before and after it, the rows a grouped call must leave untouched
+are checked bit for bit, and so are the guard bands."""
 import numpy as np
 import torch
 
@@ -47,10 +48,24 @@ def _apply(plan, sms):
     fg.fg_set_swap_mode(swap)
 
 
+GUARD = 4096  # canary elements on each side of D
+
+
 def _empty(shape, f32):
+    """D filled with the sentinel, inside a buffer whose GUARD elements before
+    and after it hold the sentinel too (checked by _guards_intact)."""
+    n = int(np.prod(shape))
     if f32:
-        return torch.full(shape, SENT32, dtype=torch.int32, device="cuda").view(torch.float32)
-    return torch.full(shape, -1, dtype=torch.int16, device="cuda").view(torch.bfloat16)
+        buf = torch.full((GUARD + n + GUARD,), SENT32, dtype=torch.int32, device="cuda")
+        return buf[GUARD:GUARD + n].view(torch.float32).view(shape), buf
+    buf = torch.full((GUARD + n + GUARD,), -1, dtype=torch.int16, device="cuda")
+    return buf[GUARD:GUARD + n].view(torch.bfloat16).view(shape), buf
+
+
+def _guards_intact(buf, f32):
+    host = buf.cpu().numpy()
+    want = SENT32 if f32 else -1
+    return bool(np.all(host[:GUARD] == want) and np.all(host[-GUARD:] == want))
 
 
 def _check(D, f32, ref16, ref64, written, what):
@@ -95,7 +110,7 @@ def random_case(case, rng_base, seed_base):
         p = wl.dense(m, n, k, seed=seed, b_fmt=b_fmt, a_fmt=a_fmt)
         plan = _draw_plan(rng, layout, m, k)
         _apply(plan, sms)
-        D = _empty((m, n), f32)
+        D, buf = _empty((m, n), f32)
         getattr(fg, "fg_gemm_fp8_nt" + sfx)(dev(p.A, fp8_dtype(a_fmt)), fg.fg_scales_a_to_mn_major(dev(p.sA)),
                                             dev(p.B, fp8_dtype(b_fmt)), dev(p.sB), D)
         ref16, ref64 = oracle.gemm_fp8_nt(p.A, a_fmt, p.sA, p.B, b_fmt, p.sB, want_f64=f32)
@@ -109,7 +124,7 @@ def random_case(case, rng_base, seed_base):
             return False
         plan = _draw_plan(rng, layout, p.M, k)
         _apply(plan, sms)
-        D = _empty((p.M, n), f32)
+        D, buf = _empty((p.M, n), f32)
         getattr(fg, "fg_grouped_gemm_fp8_contiguous" + sfx)(
             dev(p.A, fp8_dtype(p.a_fmt)), fg.fg_scales_a_to_mn_major(dev(p.sA)), dev(p.B, fp8_dtype(b_fmt)),
             dev(p.sB), D, dev(p.m_indices))
@@ -124,7 +139,7 @@ def random_case(case, rng_base, seed_base):
         p = wl.masked(G, M_cap, n=n, k=k, seed=seed, masked_m=counts, b_fmt=b_fmt)
         plan = _draw_plan(rng, layout, M_cap, k)
         _apply(plan, sms)
-        D = _empty((G, M_cap, n), f32)
+        D, buf = _empty((G, M_cap, n), f32)
         getattr(fg, "fg_grouped_gemm_fp8_masked" + sfx)(
             dev(p.A, fp8_dtype(p.a_fmt)), fg.fg_scales_a_to_mn_major(dev(p.sA)), dev(p.B, fp8_dtype(b_fmt)),
             dev(p.sB), D, dev(p.masked_m))
@@ -138,7 +153,7 @@ def random_case(case, rng_base, seed_base):
         p = wl.k_grouped(M, n, ks, seed=seed, b_fmt=b_fmt, K=K)
         plan = _draw_plan(rng, layout, M, K)
         _apply(plan, sms)
-        D = _empty((G, M, n), f32)
+        D, buf = _empty((G, M, n), f32)
         getattr(fg, "fg_k_grouped_gemm_fp8_nt" + sfx)(
             dev(p.A, fp8_dtype(p.a_fmt)), fg.fg_scales_a_to_mn_major(dev(p.sA)), dev(p.B, fp8_dtype(b_fmt)),
             dev(p.sB), D, dev(np.array(ks, np.int32)))
@@ -146,6 +161,7 @@ def random_case(case, rng_base, seed_base):
         written = np.ones((G, M, n), bool)
     torch.cuda.synchronize()
     check_status()
+    assert _guards_intact(buf, f32), f"case {case}: bytes outside D were written"
     what = (f"case {case}: {layout} {tuple(D.shape)} k={p.k} B fmt {b_fmt} {'f32' if f32 else 'bf16'} plan {plan} "
             f"sms {sms}")
     _check(D, f32, ref16, ref64, written, what)
