@@ -1,7 +1,7 @@
 """Seeded random calls of the four GEMM layouts, shared by the randomized
 parity sweeps of the release library and of the FG_DEBUG build: each draw
-picks the shape (ragged in every dimension), the FP8 format of B (and of A for
-dense calls), the output type and a tile plan forced through the process-wide
+picks the shape (ragged in every dimension), the FP8 formats of A and B, the
+output type and a tile plan forced through the process-wide
 knobs, runs the call through the C ABI and compares every output element with
 the CPU oracle; D starts filled with a sentinel inside a buffer with sentinel
 guard bands before and after it, the rows a grouped call must leave untouched
@@ -96,6 +96,7 @@ def random_case(case, rng_base, seed_base):
     rng = np.random.default_rng(rng_base + case)
     layout = LAYOUTS[case % len(LAYOUTS)]
     b_fmt = wl.E5M2 if rng.random() < 0.3 else wl.E4M3
+    a_fmt = wl.E5M2 if rng.random() < 0.2 else wl.E4M3
     f32 = bool(rng.random() < 0.3)
     n = 8 * int(rng.integers(1, 161))
     seed = wl.seed_for(9, seed_base + case)
@@ -106,7 +107,6 @@ def random_case(case, rng_base, seed_base):
 
     if layout == "dense":
         m, k = int(rng.integers(1, 1101)), 16 * int(rng.integers(1, 151))
-        a_fmt = wl.E5M2 if rng.random() < 0.2 else wl.E4M3
         p = wl.dense(m, n, k, seed=seed, b_fmt=b_fmt, a_fmt=a_fmt)
         plan = _draw_plan(rng, layout, m, k)
         _apply(plan, sms)
@@ -119,7 +119,7 @@ def random_case(case, rng_base, seed_base):
         G = int(rng.integers(1, 6))
         rows = [int(rng.integers(0, 301)) for _ in range(G)]
         k = 16 * int(rng.integers(1, 76))
-        p = wl.contiguous(rows, n=n, k=k, seed=seed, b_fmt=b_fmt)
+        p = wl.contiguous(rows, n=n, k=k, seed=seed, b_fmt=b_fmt, a_fmt=a_fmt)
         if p.M == 0:
             return False
         plan = _draw_plan(rng, layout, p.M, k)
@@ -136,7 +136,7 @@ def random_case(case, rng_base, seed_base):
         G, M_cap = int(rng.integers(1, 6)), int(rng.integers(1, 401))
         k = 16 * int(rng.integers(1, 76))
         counts = [int(rng.choice([0, M_cap, int(rng.integers(0, M_cap + 1))])) for _ in range(G)]
-        p = wl.masked(G, M_cap, n=n, k=k, seed=seed, masked_m=counts, b_fmt=b_fmt)
+        p = wl.masked(G, M_cap, n=n, k=k, seed=seed, masked_m=counts, b_fmt=b_fmt, a_fmt=a_fmt)
         plan = _draw_plan(rng, layout, M_cap, k)
         _apply(plan, sms)
         D, buf = _empty((G, M_cap, n), f32)
@@ -150,7 +150,7 @@ def random_case(case, rng_base, seed_base):
         G, M = int(rng.integers(1, 7)), int(rng.integers(1, 601))
         ks = [128 * int(rng.integers(0, 7)) for _ in range(G)]
         K = sum(ks) + 16 * int(rng.integers(0 if sum(ks) else 1, 11))
-        p = wl.k_grouped(M, n, ks, seed=seed, b_fmt=b_fmt, K=K)
+        p = wl.k_grouped(M, n, ks, seed=seed, b_fmt=b_fmt, K=K, a_fmt=a_fmt)
         plan = _draw_plan(rng, layout, M, K)
         _apply(plan, sms)
         D, buf = _empty((G, M, n), f32)
@@ -162,7 +162,7 @@ def random_case(case, rng_base, seed_base):
     torch.cuda.synchronize()
     check_status()
     assert _guards_intact(buf, f32), f"case {case}: bytes outside D were written"
-    what = (f"case {case}: {layout} {tuple(D.shape)} k={p.k} B fmt {b_fmt} {'f32' if f32 else 'bf16'} plan {plan} "
+    what = (f"case {case}: {layout} {tuple(D.shape)} k={p.k} A/B fmt {a_fmt}/{b_fmt} {'f32' if f32 else 'bf16'} plan {plan} "
             f"sms {sms}")
     _check(D, f32, ref16, ref64, written, what)
     return True

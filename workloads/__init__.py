@@ -208,7 +208,7 @@ class Contiguous:
                 + used * nb * kb * 4 + self.valid_rows * self.n * 2 + self.M * 4)
 
 
-def contiguous(group_rows, n, k, seed, b_fmt=E4M3, align=MBLOCK_ALIGN) -> Contiguous:
+def contiguous(group_rows, n, k, seed, b_fmt=E4M3, align=MBLOCK_ALIGN, a_fmt=E4M3) -> Contiguous:
     """Contiguous layout: group g contributes group_rows[g] rows, each segment
     padded with -1 rows to a multiple of `align`, segments concatenated on M."""
     rng = rng_for(seed)
@@ -220,13 +220,13 @@ def contiguous(group_rows, n, k, seed, b_fmt=E4M3, align=MBLOCK_ALIGN) -> Contig
     for g, (r, s) in enumerate(zip(group_rows, seg)):
         m_indices[r0:r0 + r] = g
         r0 += s
-    A, sA = _quant_rows_chunked(rng, M, k, E4M3) if M > 0 else (
+    A, sA = _quant_rows_chunked(rng, M, k, a_fmt) if M > 0 else (
         np.zeros((0, k), np.uint8), np.zeros((0, cdiv(k, KBLOCK)), np.float32))
     B = np.empty((G, n, k), np.uint8)
     sB = np.empty((G, cdiv(n, NBLOCK), cdiv(k, KBLOCK)), np.float32)
     for g in range(G):
         B[g], sB[g] = _quant_blocks_chunked(rng, n, k, b_fmt)
-    return Contiguous(M, n, k, G, A, sA, B, sB, m_indices, list(group_rows), E4M3, b_fmt, seed)
+    return Contiguous(M, n, k, G, A, sA, B, sB, m_indices, list(group_rows), a_fmt, b_fmt, seed)
 
 
 @dataclass
@@ -262,20 +262,20 @@ class Masked:
                 + v * self.n * 2 + self.G * 4)
 
 
-def masked(G, M_cap, n, k, seed, masked_m=None, b_fmt=E4M3) -> Masked:
+def masked(G, M_cap, n, k, seed, masked_m=None, b_fmt=E4M3, a_fmt=E4M3) -> Masked:
     """Masked layout: fixed capacity M_cap per group; valid-row counts drawn
     uniformly from [0, M_cap] (inclusive) unless given."""
     rng = rng_for(seed)
     if masked_m is None:
         masked_m = rng.integers(0, M_cap, size=G, endpoint=True)
     masked_m = np.asarray(masked_m, np.int32)
-    A, sA = _quant_rows_chunked(rng, G * M_cap, k, E4M3)
+    A, sA = _quant_rows_chunked(rng, G * M_cap, k, a_fmt)
     B = np.empty((G, n, k), np.uint8)
     sB = np.empty((G, cdiv(n, NBLOCK), cdiv(k, KBLOCK)), np.float32)
     for g in range(G):
         B[g], sB[g] = _quant_blocks_chunked(rng, n, k, b_fmt)
     return Masked(G, M_cap, n, k, A.reshape(G, M_cap, k), sA.reshape(G, M_cap, -1),
-                  B, sB, masked_m, E4M3, b_fmt, seed)
+                  B, sB, masked_m, a_fmt, b_fmt, seed)
 
 
 # ------------------------------------------------- the five named workloads
@@ -376,9 +376,9 @@ def k_grouped_short_shapes():
     return [(KGROUPED_SHORT_G, n, k, KGROUPED_SHORT_TOKENS) for (n, k) in GROUPED_NK]
 
 
-def k_grouped(M, N, k_sizes, seed, b_fmt=E4M3, K=None) -> Dense:
+def k_grouped(M, N, k_sizes, seed, b_fmt=E4M3, K=None, a_fmt=E4M3) -> Dense:
     """Operands of a K-grouped problem: A [M][K], B [N][K] with the NT GEMM's
     scaling (1 x 128 LHS groups, 128 x 128 RHS blocks), K = sum of the segment
     lengths unless given.  Returns a Dense holding them (m = M, n = N, k = K)."""
     total = int(np.sum(k_sizes))
-    return dense(M, N, total if K is None else K, seed, b_fmt=b_fmt)
+    return dense(M, N, total if K is None else K, seed, b_fmt=b_fmt, a_fmt=a_fmt)
