@@ -218,6 +218,9 @@ def barrier(ws):
 
 # ------------------------------------------------------------ CPU oracle
 
+_ORACLE_CALIB = {}
+
+
 def oracle_sample_rate(probs, shapes, seconds: float, seed: int = 0):
     """Time the CPU oracle (as it stands) on a bounded sample of the sweep:
     the same number of random output elements of every problem, sized for
@@ -237,8 +240,15 @@ def oracle_sample_rate(probs, shapes, seconds: float, seed: int = 0):
             flops += 2.0 * k * per_shape
         return flops, time.perf_counter() - t0
 
-    f0, t0 = run(256)  # calibration
-    per = int(max(64, min(1 << 22, 256 * seconds / max(t0, 1e-6))))
+    # calibration (once per process): grow the sample until the fixed cost of
+    # a call (thread start-up, Python) no longer dominates, then scale to `seconds`
+    if "s_per_elem" not in _ORACLE_CALIB:
+        per, (f0, t0) = 256, run(256)
+        while t0 < 0.5 and per < (1 << 20):
+            per *= 4
+            f0, t0 = run(per)
+        _ORACLE_CALIB["s_per_elem"] = t0 / per
+    per = int(max(64, min(1 << 22, seconds / max(_ORACLE_CALIB["s_per_elem"], 1e-12))))
     f, t = run(per)
     sample = (f"{per} random output elements of each of the {len(shapes)} sweep problems "
               f"({f / 2e9:.1f} G MAC, {t:.1f} s)")
