@@ -141,6 +141,27 @@ def test_quantize_argument_checks():
     assert call(rows=0) == 0              # nothing to do: no launch
 
 
+def test_quantize_f32_input_argument_checks():
+    """fg_quantize_fp8_per_token_f32in applies the same host checks, with the
+    row alignment of 4-byte elements (ld_x % 4 == 0 instead of % 8)."""
+    Q = fg.lib().fg_quantize_fp8_per_token_f32in
+    ok = [FAKE, 256, 0, FAKE, FAKE, 64, None, 1, 64, 256, None]
+
+    def call(**kw):
+        names = ["X", "ld_x", "fmt", "A", "sA", "ld_sA", "masked", "batches", "rows", "k", "stream"]
+        args = dict(zip(names, ok))
+        args.update(kw)
+        return Q(*[args[n] for n in names])
+
+    assert call(X=None) == 1 and call(A=None) == 1 and call(sA=None) == 1
+    assert call(fmt=2) == 1 and call(ld_x=128) == 1 and call(ld_sA=60) == 1
+    assert call(X=FAKE + 8) == 2 and call(A=FAKE + 8) == 2
+    assert call(ld_x=258) == 2            # 1032-byte rows: not 16-byte aligned
+    assert call(ld_x=260, rows=0) == 0    # 1040-byte rows are (a BF16 X of this ld_x is not)
+    assert call(k=136, ld_x=136) == 3
+    assert call(rows=0) == 0
+
+
 def test_f32out_argument_checks():
     """The FP32-output calls share the BF16 calls' host-side checks."""
     L = fg.lib()
